@@ -1,0 +1,218 @@
+/*
+ * qdq_oracle.c -- plain, slow CPU oracle for block-quantised dequantisation and
+ * the dequant-GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY. The tests, the smoke check and the benchmark's
+ * CPU-baseline leg may call it; the library's compute path never does. It shares
+ * no code, header or table with the CUDA path.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC
+ * (-ffp-contract=off matters: on aarch64 gcc would otherwise fuse a*b-c into one
+ * FMA and change the rounding the pages fix.)
+ *
+ * Every float operation below is one IEEE-754 binary32 operation in the order the
+ * cited passage evaluates it. No blocking, fusion or reordering.
+ *
+ * Sources (page title, section):
+ *   [S21]  "S21 The Capstone: picoLM, in Python", section 2 "K-quants"
+ *          (Q4_K super-block diagram and dequantize_q4_K), section 3 (fused
+ *          dequant + dot; the unfused reference path is dequantise-then-dot).
+ *   [Q6K]  "PicoLM Q6_K quantisation bug" (block_q6_K struct; one int8 scale per
+ *          16 weights; scale group = is + l/16; y = d * sc * q).
+ *   [PETIT] "PETIT -- a tiny, CPU-first, quantized LLM inference engine",
+ *          "What makes it fast & small" and "How the pieces match" (q8_0 = fp32
+ *          scale + 32 int8; q4_0 = fp16 scale + 16 nibble bytes; weights stored
+ *          out x in, one projection = one gemv).
+ *
+ * Pin status (what the tests hold each function to):
+ *   fp16 -> fp32    pinned: all 65536 patterns vs numpy float16.
+ *   Q4_K            pinned: hand-built blocks with closed-form values, the
+ *                   12-byte scale/min field layout, mutations.
+ *   Q6_K            pinned: struct offsets, one scale per 16 weights, the
+ *                   scale[0]/scale[1] error ratio, closed forms. The placement
+ *                   of each quant's 4 low bits in ql and 2 high bits in qh is
+ *                   NOT printed on the pages: it follows the ggml layout (a
+ *                   reading), and is "parity unpinned" against the pages.
+ *   q8_0, q4_0      pinned: hand-built blocks with closed-form values. The q4_0
+ *                   nibble order (low nibble = weight i, high = weight i+16) is
+ *                   the workload definition's reading.
+ *   GEMV            pinned: exact rational sums on tiny inputs, unit-vector
+ *                   columns (catches a transposed operand), closed forms.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { ORC_Q4_0 = 1, ORC_Q8_0 = 2, ORC_Q4_K = 3, ORC_Q6_K = 4 };
+
+/* ---- IEEE-754 binary16 -> binary32, from the format definition ---------------
+ * sign s (1 bit), exponent e (5 bits, bias 15), fraction f (10 bits):
+ *   e == 0        : (-1)^s * f * 2^-24          (zero, subnormal)
+ *   0 < e < 31    : (-1)^s * (1024 + f) * 2^(e-25)
+ *   e == 31       : f == 0 ? (-1)^s * inf : NaN
+ * Every binary16 value is exactly representable in binary32.                    */
+float orc_fp16_to_fp32(uint16_t h) {
+    unsigned s = (h >> 15) & 1u, e = (h >> 10) & 31u, f = h & 1023u;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? (double)NAN : (double)INFINITY;
+    else
+        v = ldexp((double)(1024u + f), (int)e - 25);
+    return (float)(s ? -v : v);
+}
+
+static float rd_fp16(const uint8_t *p) { return orc_fp16_to_fp32((uint16_t)(p[0] | (p[1] << 8))); }
+
+/* ---- Q4_K: 144 bytes -> 256 weights [S21 section 2] ----------------------------
+ * bytes 0-1 fp16 d, 2-3 fp16 dmin, 4-15 the packed 6-bit scale/min fields,
+ * 16-143 the nibbles. Field j of the eight (sub-block j, 32 weights each):
+ *   j < 4 : the field sits in the low six bits of its own byte:
+ *           sc = p[j] & 63,            mn = p[j+4] & 63
+ *   j >= 4: low four bits from p[j+4], top two bits from bits 6-7 of an earlier
+ *           byte:
+ *           sc = (p[j+4] & 15) | (p[j-4] >> 6) << 4
+ *           mn = (p[j+4] >> 4) | (p[j]   >> 6) << 4                            */
+void orc_q4k_scale_min(const uint8_t *p, int j, int *sc, int *mn) {
+    if (j < 4) {
+        *sc = p[j] & 63;
+        *mn = p[j + 4] & 63;
+    } else {
+        *sc = (p[j + 4] & 15) | ((p[j - 4] >> 6) << 4);
+        *mn = (p[j + 4] >> 4) | ((p[j] >> 6) << 4);
+    }
+}
+
+/* The nibble bytes form four chunks of 32 bytes. In chunk c the low nibbles are
+ * weights 64c..64c+31 (sub-block 2c) and the high nibbles are weights
+ * 64c+32..64c+63 (sub-block 2c+1). Value, evaluated left to right as the page's
+ * NumPy expression does: (d * sc) * q - (dmin * mn).                            */
+void orc_dequant_q4_K_block(const uint8_t *blk, float *out) {
+    float d = rd_fp16(blk), dmin = rd_fp16(blk + 2);
+    const uint8_t *p = blk + 4, *qs = blk + 16;
+    for (int e = 0; e < 256; ++e) {
+        int c = e / 64, i = e % 64;
+        int s = 2 * c + (i >= 32);
+        int q = (i < 32) ? (qs[32 * c + i] & 15) : (qs[32 * c + i - 32] >> 4);
+        int sc, mn;
+        orc_q4k_scale_min(p, s, &sc, &mn);
+        float a = d * (float)sc;
+        a = a * (float)q;
+        float b = dmin * (float)mn;
+        out[e] = a - b;
+    }
+}
+
+/* ---- Q6_K: 210 bytes -> 256 weights [Q6K] -------------------------------------
+ * struct { uint8 ql[128]; uint8 qh[64]; int8 scales[16]; fp16 d; }.
+ * Each quant has six bits: four in ql, two in qh (placement: ggml layout, a
+ * reading -- see the header). Element e = 128h + 32k + l (h = half, k = 0..3,
+ * l = 0..31):
+ *   low  = ql[64h + 32(k & 1) + l], low nibble for k < 2, high nibble for k >= 2
+ *   high = (qh[32h + l] >> 2k) & 3
+ *   q    = (low | high << 4) - 32
+ * One scale per 16 weights: element e uses scales[e / 16]. This is the fixed
+ * rule "is + l/16" of the page: with is = 8h, y[l], y[l+32], y[l+64], y[l+96]
+ * take sc[is + l/16 + 0, 2, 4, 6].
+ * Value, left to right as the page's C: (d * sc) * q.                           */
+void orc_dequant_q6_K_block(const uint8_t *blk, float *out) {
+    const uint8_t *ql = blk, *qh = blk + 128;
+    const int8_t *scales = (const int8_t *)(blk + 192);
+    float d = rd_fp16(blk + 208);
+    for (int e = 0; e < 256; ++e) {
+        int h = e / 128, k = (e % 128) / 32, l = e % 32;
+        int lb = ql[64 * h + 32 * (k & 1) + l];
+        int low = (k < 2) ? (lb & 15) : (lb >> 4);
+        int high = (qh[32 * h + l] >> (2 * k)) & 3;
+        int q = (low | (high << 4)) - 32;
+        float a = d * (float)scales[e / 16];
+        out[e] = a * (float)q;
+    }
+}
+
+/* ---- PETIT q8_0: 36 bytes -> 32 weights [PETIT] --------------------------------
+ * fp32 scale d, then 32 int8 q. w = d * q (one rounding).                       */
+void orc_dequant_q8_0_block(const uint8_t *blk, float *out) {
+    float d;
+    memcpy(&d, blk, 4); /* little-endian host; the format is little-endian */
+    const int8_t *q = (const int8_t *)(blk + 4);
+    for (int i = 0; i < 32; ++i) out[i] = d * (float)q[i];
+}
+
+/* ---- PETIT q4_0: 18 bytes -> 32 weights [PETIT] --------------------------------
+ * fp16 scale d, then 16 bytes; byte i holds weight i in its low nibble and
+ * weight i+16 in its high nibble; w = (q - 8) * d (one rounding).               */
+void orc_dequant_q4_0_block(const uint8_t *blk, float *out) {
+    float d = rd_fp16(blk);
+    const uint8_t *qs = blk + 2;
+    for (int i = 0; i < 32; ++i) {
+        int q = (i < 16) ? (qs[i] & 15) : (qs[i - 16] >> 4);
+        out[i] = (float)(q - 8) * d;
+    }
+}
+
+int orc_block_bytes(int type) {
+    switch (type) {
+    case ORC_Q4_0: return 18;
+    case ORC_Q8_0: return 36;
+    case ORC_Q4_K: return 144;
+    case ORC_Q6_K: return 210;
+    default: return -1;
+    }
+}
+
+int orc_block_weights(int type) {
+    switch (type) {
+    case ORC_Q4_0: case ORC_Q8_0: return 32;
+    case ORC_Q4_K: case ORC_Q6_K: return 256;
+    default: return -1;
+    }
+}
+
+/* Dequantise n weights (n a multiple of the block size). Returns 0, or -1 on a
+ * bad type or size.                                                            */
+int orc_dequant(int type, const uint8_t *blocks, int64_t n, float *out) {
+    int bw = orc_block_weights(type), bb = orc_block_bytes(type);
+    if (bw < 0 || n < 0 || n % bw) return -1;
+    for (int64_t b = 0; b < n / bw; ++b) {
+        const uint8_t *blk = blocks + b * bb;
+        float *o = out + b * bw;
+        switch (type) {
+        case ORC_Q4_K: orc_dequant_q4_K_block(blk, o); break;
+        case ORC_Q6_K: orc_dequant_q6_K_block(blk, o); break;
+        case ORC_Q8_0: orc_dequant_q8_0_block(blk, o); break;
+        case ORC_Q4_0: orc_dequant_q4_0_block(blk, o); break;
+        }
+    }
+    return 0;
+}
+
+/* ---- GEMV: the unfused definition [S21 section 3; PETIT] ----------------------
+ * W is rows x cols (out x in), row-major, each row cols/QK whole blocks.
+ * x is [batch][cols], y and S are [batch][rows]. For each row: dequantise the row
+ * to fp32 exactly as above, then in double precision
+ *   y[b][r] = sum_c w[r][c] * x[b][c]      S[b][r] = sum_c |w[r][c] * x[b][c]|
+ * summed in column order. Each double product of two floats is exact.
+ * `row_buf` holds cols floats. Rows [r0, r1) only, so callers can sample.      */
+int orc_gemv_rows(int type, const uint8_t *W, int64_t rows, int64_t cols, const float *x,
+                  int batch, int64_t r0, int64_t r1, double *y, double *S, float *row_buf) {
+    int bw = orc_block_weights(type), bb = orc_block_bytes(type);
+    if (bw < 0 || cols % bw || rows < 0 || batch < 1 || r0 < 0 || r1 > rows || r0 > r1) return -1;
+    int64_t rbytes = (cols / bw) * bb;
+    for (int64_t r = r0; r < r1; ++r) {
+        if (orc_dequant(type, W + r * rbytes, cols, row_buf)) return -1;
+        for (int b = 0; b < batch; ++b) {
+            const float *xb = x + (int64_t)b * cols;
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t c = 0; c < cols; ++c) {
+                double p = (double)row_buf[c] * (double)xb[c];
+                acc += p;
+                sabs += fabs(p);
+            }
+            y[(int64_t)b * rows + r] = acc;
+            S[(int64_t)b * rows + r] = sabs;
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs: raw quantised blocks and fp32 activation vectors.
+
+This module only lays random numbers out at the byte offsets of each block
+format. It holds none of the decode or dot-product arithmetic, so both the CPU
+oracle tests and the CUDA path can take their inputs from it.
+
+Why uniform random bytes are the right draw:
+
+* Q4_K ("S21 The Capstone: picoLM, in Python", section 2, the Q4_K super-block
+  diagram and dequantize_q4_K): bytes 4..15 pack eight 6-bit scales and eight
+  6-bit mins. Every one of the 96 bits belongs to exactly one field, so uniform
+  random bytes give independent uniform fields in 0..63. The 128 nibble bytes
+  give independent uniform nibbles in 0..15.
+* Q6_K ("PicoLM Q6_K quantisation bug", the block_q6_K struct): ql[128] and
+  qh[64] hold disjoint bits of each 6-bit quant, so random bytes give uniform
+  quants in 0..63. scales[16] read as int8 are then uniform in -128..127.
+* PETIT q4_0 ("PETIT", "How the pieces match"): fp16 scale + 16 nibble bytes.
+* PETIT q8_0 (same section): fp32 scale + 32 int8, drawn in -127..127.
+
+The scales d (and dmin) are drawn from U[1e-4, 1e-2] and rounded to fp16 by
+numpy (round to nearest even); q8_0 keeps its scale in fp32.
+"""
+from __future__ import annotations
+
+import hashlib
+from dataclasses import dataclass
+
+import numpy as np
+
+# Type codes of the C ABI (include/qdq.h).
+Q4_0 = 1
+Q8_0 = 2  # PETIT q8_0: fp32 scale + 32 int8
+Q4_K = 3
+Q6_K = 4
+
+TYPE_NAMES = {Q4_0: "q4_0", Q8_0: "q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K"}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210}
+BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256}
+
+SCALE_LO, SCALE_HI = 1e-4, 1e-2
+
+
+def row_bytes(qtype: int, cols: int) -> int:
+    return (cols // BLOCK_WEIGHTS[qtype]) * BLOCK_BYTES[qtype]
+
+
+def _fp16_bytes(v: np.ndarray) -> np.ndarray:
+    return v.astype("<f2").view(np.uint8).reshape(-1, 2)
+
+
+def gen_blocks(qtype: int, nblocks: int, rng: np.random.Generator) -> np.ndarray:
+    """Return `nblocks` random blocks of `qtype` as a flat uint8 array."""
+    bb = BLOCK_BYTES[qtype]
+    out = np.empty((nblocks, bb), dtype=np.uint8)
+    if qtype == Q4_K:
+        d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
+        dmin = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
+        out[:, 0:2] = _fp16_bytes(d)
+        out[:, 2:4] = _fp16_bytes(dmin)
+        out[:, 4:144] = rng.integers(0, 256, (nblocks, 140), dtype=np.uint8)
+    elif qtype == Q6_K:
+        d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
+        out[:, 0:208] = rng.integers(0, 256, (nblocks, 208), dtype=np.uint8)
+        out[:, 208:210] = _fp16_bytes(d)
+    elif qtype == Q8_0:
+        d = rng.uniform(SCALE_LO, SCALE_HI, nblocks).astype("<f4")
+        out[:, 0:4] = d.view(np.uint8).reshape(-1, 4)
+        out[:, 4:36] = rng.integers(-127, 128, (nblocks, 32)).astype(np.int8).view(np.uint8)
+    elif qtype == Q4_0:
+        d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
+        out[:, 0:2] = _fp16_bytes(d)
+        out[:, 2:18] = rng.integers(0, 256, (nblocks, 16), dtype=np.uint8)
+    else:
+        raise ValueError(f"unknown block type {qtype}")
+    return out.reshape(-1)
+
+
+def gen_matrix(qtype: int, rows: int, cols: int, seed: int) -> np.ndarray:
+    """A rows x cols weight matrix: row-major, each row a run of whole blocks."""
+    if cols % BLOCK_WEIGHTS[qtype]:
+        raise ValueError("cols must be a multiple of the block size")
+    rng = np.random.default_rng(seed)
+    return gen_blocks(qtype, rows * (cols // BLOCK_WEIGHTS[qtype]), rng)
+
+
+def gen_x(batch: int, cols: int, seed: int) -> np.ndarray:
+    """Activations x ~ N(0, 1), fp32, laid out [batch][cols]."""
+    rng = np.random.default_rng(seed)
+    return rng.standard_normal((batch, cols), dtype=np.float32)
+
+
+def digest(a: np.ndarray) -> str:
+    return hashlib.sha256(np.ascontiguousarray(a).view(np.uint8)).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------------------
+# Workload shapes. Seeds: tensor t of a workload uses seed base + t, and its
+# activation vector uses seed base + 1000 + t.
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Gemv:
+    name: str
+    qtype: int
+    rows: int
+    cols: int
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.rows * row_bytes(self.qtype, self.cols)
+
+
+# Single GEMVs.
+Q4K_2048x2048 = Gemv("Q4_K 2048x2048", Q4_K, 2048, 2048)
+Q6K_2048x5632 = Gemv("Q6_K 2048x5632 (ffn_down)", Q6_K, 2048, 5632)
+
+# 1.1B Llama shape, Q4_K_M mix: hidden 2048, 32 q heads / 4 kv heads of 64,
+# FFN 5632, vocab 32000, 22 layers.
+LLAMA_1B = dict(n_layers=22, hidden=2048, n_heads=32, n_kv_heads=4, head_dim=64,
+                ffn=5632, vocab=32000)
+
+
+def llama_1b_layer(l: int) -> list[Gemv]:
+    h, kv, f = 2048, 4 * 64, 5632
+    return [
+        Gemv(f"blk.{l}.attn_q", Q4_K, h, h),
+        Gemv(f"blk.{l}.attn_k", Q4_K, kv, h),
+        Gemv(f"blk.{l}.attn_v", Q6_K, kv, h),
+        Gemv(f"blk.{l}.attn_output", Q4_K, h, h),
+        Gemv(f"blk.{l}.ffn_gate", Q4_K, f, h),
+        Gemv(f"blk.{l}.ffn_up", Q4_K, f, h),
+        Gemv(f"blk.{l}.ffn_down", Q6_K, h, f),
+    ]
+
+
+def llama_1b_step(n_layers: int = 22) -> list[list[Gemv]]:
+    """The GEMVs of one decode step, grouped into dependency levels.
+
+    Within a level the GEMVs read the same input vector in a real forward pass
+    ({q,k,v} read rmsnorm(x); {gate,up} read rmsnorm(h)); each level depends on
+    the previous one. The output head is the last level.
+    """
+    levels: list[list[Gemv]] = []
+    for l in range(n_layers):
+        q, k, v, o, g, u, d = llama_1b_layer(l)
+        levels += [[q, k, v], [o], [g, u], [d]]
+    levels.append([Gemv("output", Q6_K, LLAMA_1B["vocab"], LLAMA_1B["hidden"])])
+    return levels
+
+
+def step_weight_bytes(levels: list[list[Gemv]]) -> int:
+    return sum(g.weight_bytes for lv in levels for g in lv)
