@@ -1,0 +1,380 @@
+"""Benchmark: the fused dequant-GEMV decode step on GB300.
+
+Default workload: one batch-1 decode step of the 1.1B Llama shape (22 layers,
+hidden 2048, 32/4 heads of 64, FFN 5632, vocab 32000; Q4_K for attn_q/k/o and
+ffn_gate/up, Q6_K for attn_v, ffn_down and the output head), seeded random
+blocks, a fresh N(0,1) input per dependency level. One step = one persistent
+launch of the plan (155 GEMVs in 89 dependency levels). The 667 MB of weights
+exceed the 129 MB L2 several times over, so no flush is needed between steps.
+
+Prints one JSON line. `value` is HBM GB/s of algorithmic bytes (weights + x + y
+per step) over the device-timed step; `tok_s` is steps per second.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload step|q4k|q6k|ffn_q4k|ffn_q6k|q8_0|q4_0] [--batch B]
+Under torchrun each rank runs an independent replica (the path has no data
+exchange); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from quant_dequant_gemv_gb300 import synth  # noqa: E402
+
+METRIC = "fused dequant-GEMV HBM GB/s (% of GB300 peak); 1.1B-shape decode-step tok/s"
+
+WORKLOADS = {
+    "step": "1.1B Llama-shape decode step, batch 1: 22 layers, Q4_K_M mix (Q4_K attn_q/k/o, ffn_gate/up; "
+            "Q6_K attn_v, ffn_down, output 32000x2048), 155 GEMVs in 89 dependency levels, "
+            "667,152,384 weight bytes",
+    "q4k": "single Q4_K GEMV 2048x2048",
+    "q6k": "single Q6_K GEMV 2048x5632",
+    "ffn_q4k": "Q4_K GEMV 5632x2048 (ffn_gate/up shape)",
+    "ffn_q6k": "Q6_K GEMV 2048x5632 (ffn_down shape)",
+    "q8_0": "PETIT q8_0 GEMVs 14336x4096 and 4096x14336",
+    "q4_0": "PETIT q4_0 GEMVs 14336x4096 and 4096x14336",
+}
+
+
+def workload_levels(name: str) -> list[list[synth.Gemv]]:
+    if name == "step":
+        return synth.llama_1b_step(22)
+    if name == "q4k":
+        return [[synth.Q4K_2048x2048]]
+    if name == "q6k":
+        return [[synth.Q6K_2048x5632]]
+    if name == "ffn_q4k":
+        return [[synth.Gemv("ffn_gate", synth.Q4_K, 5632, 2048)]]
+    if name == "ffn_q6k":
+        return [[synth.Gemv("ffn_down", synth.Q6_K, 2048, 5632)]]
+    if name in ("q8_0", "q4_0"):
+        t = synth.Q8_0 if name == "q8_0" else synth.Q4_0
+        return [[synth.Gemv("w_up", t, 14336, 4096)], [synth.Gemv("w_down", t, 4096, 14336)]]
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_bytes(levels, batch: int) -> int:
+    """Weights once, each level's x once, every y once."""
+    w = sum(g.weight_bytes for lv in levels for g in lv)
+    x = sum(4 * batch * lv[0].cols for lv in levels)
+    y = sum(4 * batch * g.rows for lv in levels for g in lv)
+    return w + x + y
+
+
+def load_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "quant_dequant_gemv_gb300" / "csrc").glob("*")):
+        h.update(f.read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, batch: int):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    p = ROOT / "profiles" / "dram_traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text())
+    e = d.get(f"{workload}/b{batch}")
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the GPU is under load."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        for line in Path(self.file.name).read_text().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        reasons = set()
+        for _, _, hw, hwt, swt, swp in rows:
+            if hw == "Active":
+                reasons.add("hw_slowdown")
+            if hwt == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if swt == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if swp == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def build_inputs(levels, batch, device, seed=0):
+    import torch
+    items, lv, xs_host = [], [], []
+    for li, level in enumerate(levels):
+        x = synth.gen_x(batch, level[0].cols, seed + 1000 + li)
+        xs_host.append(x)
+        xd = torch.from_numpy(x).to(device)
+        for gi, g in enumerate(level):
+            W = synth.gen_matrix(g.qtype, g.rows, g.cols, seed + 10 * li + gi)
+            y = torch.empty(batch, g.rows, dtype=torch.float32, device=device)
+            items.append((g.qtype, torch.from_numpy(W).to(device), g.rows, g.cols, xd, y))
+            lv.append(li)
+    return items, lv, xs_host
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    from quant_dequant_gemv_gb300 import build, qdq
+
+    build.build()
+    levels = workload_levels(args.workload)
+    batch = args.batch
+    items, lv, xs_host = build_inputs(levels, batch, device)
+    plan = qdq.Plan(items, lv, batch)
+    stream = torch.cuda.current_stream(device)
+    abytes = algorithmic_bytes(levels, batch)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        plan.run(stream)
+    torch.cuda.synchronize(device)
+    rc = qdq.get_device_status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status after warm-up: {qdq.status_string(rc)}")
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    t_load = time.perf_counter()
+    while time.perf_counter() - t_load < 1.0:  # untimed load so the clock samples see a busy GPU
+        for _ in range(50):
+            plan.run(stream)
+        torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        plan.run(stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    rc = qdq.get_device_status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status after timing: {qdq.status_string(rc)}")
+
+    # end to end through the C ABI: pinned host x in, every y out, each step
+    x_host = torch.from_numpy(np.concatenate([a.reshape(-1) for a in xs_host])).pin_memory()
+    y_host = torch.empty(sum(batch * it[2] for it in items), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        plan.run_io(x_host, y_host, stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    E = max(3, K // 2)
+    te = time.perf_counter()
+    h2d = d2h = 0
+    for _ in range(E):
+        h2d, d2h = plan.run_io(x_host, y_host, stream)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - te) / E
+    barrier()
+    launches = K * plan.launches
+    plan.close()
+    return {"total_ms": total_ms, "launch_ms": launch_ms, "abytes": abytes, "clocks": clocks,
+            "e2e_s": e2e_s, "h2d": h2d, "d2h": d2h, "launches": launches}
+
+
+def time_oracle(levels, batch, budget_s):
+    """Time only the oracle calls (input generation excluded)."""
+    import oracle
+    orc = oracle.get()
+    spent, done_bytes, n = 0.0, 0, 0
+    for li, level in enumerate(levels):
+        x = synth.gen_x(batch, level[0].cols, 1000 + li)
+        for gi, g in enumerate(level):
+            W = synth.gen_matrix(g.qtype, g.rows, g.cols, 10 * li + gi)
+            ts = time.perf_counter()
+            orc.gemv(g.qtype, W, g.rows, g.cols, x)
+            spent += time.perf_counter() - ts
+            done_bytes += g.weight_bytes + 4 * batch * (g.cols + g.rows)
+            n += 1
+        if spent > budget_s:
+            break
+    return spent, done_bytes, n
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="step", choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    levels = workload_levels(args.workload)
+    abytes = algorithmic_bytes(levels, args.batch)
+    step_bytes = abytes
+
+    if args.impl == "reference":
+        # The reference arm is the CPU oracle, as it stands, on the host cores:
+        # each step is a bounded sample of the workload (its first GEMVs in step
+        # order, about 1 s of work); the metric is extrapolated per byte.
+        if rank != 0:
+            return
+        budget = 0.8
+        for _ in range(args.warmup):
+            time_oracle(levels, args.batch, 0.05)
+        spent = done = 0
+        n_last = 0
+        for _ in range(args.steps):
+            s, d, n_last = time_oracle(levels, args.batch, budget)
+            spent += s
+            done += d
+        gbs = done / spent / 1e9
+        line = {
+            "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * spent / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (oracle: f64 sums)",
+            "data": "synthetic", "tok_s": round(gbs * 1e9 / step_bytes, 4),
+            "config": {"workload": WORKLOADS[args.workload], "batch": args.batch,
+                       "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"first {n_last} GEMVs of the workload in step order per step "
+                                       f"(~{budget:.1f} s of oracle time), plain C, one thread"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    r = run_ours(args, rank, world, device)
+
+    total_ms = r["total_ms"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, r["e2e_s"]], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_s = float(t[0]), float(t[1])
+    else:
+        e2e_s = r["e2e_s"]
+    ms_step = total_ms / args.steps
+    value = world * abytes / (ms_step * 1e-3) / 1e9
+    avg_launch_ms = statistics.mean(r["launch_ms"])
+    achieved = abytes / (avg_launch_ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    traffic = recorded_traffic(args.workload, args.batch)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        spent, done, n = time_oracle(levels, args.batch, 12.0)
+        cpu = {"value": round(done / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {n} GEMVs of the workload in step order ({done / 1e6:.0f} MB of weights, "
+                         f"{spent:.1f} s), plain C oracle, one thread"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "tok_s": round(world * 1e3 / ms_step, 1),
+            "config": {"workload": WORKLOADS[args.workload], "batch": args.batch,
+                       "step_bytes": abytes,
+                       "l2": "inputs larger than L2 (weights per step exceed 129 MB)"
+                       if abytes > 4 * 129e6 else "inputs smaller than L2: figures include L2 hits",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": traffic, "peak_source": peaks["source"],
+                         "kernel": "stream_kernel (persistent plan launch)"},
+            "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * qdq.h -- C ABI of libqdq: dequantisation and fused dequant-GEMV over
+ * block-quantised weights, in hand-written CUDA for sm_103a (GB300).
+ *
+ * Block formats (all little-endian, see the per-type notes below):
+ *   QDQ_Q4_K  GGUF Q4_K, 144 bytes per 256 weights ("S21 The Capstone: picoLM,
+ *             in Python", section 2 K-quants): fp16 d, fp16 dmin, 12 bytes of
+ *             packed 6-bit scales and mins (one pair per 32-weight sub-block),
+ *             128 nibble bytes. w = d*sc*q - dmin*mn.
+ *   QDQ_Q6_K  GGUF Q6_K, 210 bytes per 256 weights ("PicoLM Q6_K quantisation
+ *             bug", block_q6_K struct): ql[128] low 4 bits, qh[64] high 2 bits,
+ *             int8 scales[16] (one per 16 weights), fp16 d. w = d*sc*(q6-32).
+ *             The ql/qh bit placement follows the ggml layout.
+ *   QDQ_Q8_0  PETIT q8_0, 36 bytes per 32 weights ("PETIT", How the pieces
+ *             match): fp32 scale d, 32 int8 q. w = d*q. (Not ggml's q8_0, whose
+ *             scale is fp16.)
+ *   QDQ_Q4_0  PETIT q4_0, 18 bytes per 32 weights (same section): fp16 scale d,
+ *             16 bytes; byte i holds weight i (low nibble) and weight i+16 (high
+ *             nibble). w = (q-8)*d.
+ *
+ * Conventions for every call:
+ *   - Pointers named W, blocks, x, y, out are DEVICE pointers (cudaMalloc'd or
+ *     managed) on the current device, 16-byte aligned. A host pointer gives
+ *     QDQ_ERR_PTR, a misaligned one QDQ_ERR_ALIGN, a NULL one QDQ_ERR_PTR.
+ *   - A weight matrix is rows x cols (out x in, "PETIT": weights stored out x in,
+ *     a projection is one gemv), row-major, each row cols/QK whole blocks.
+ *     cols must be a multiple of the block's weight count QK (the caller pads,
+ *     as PETIT's exporter does), else QDQ_ERR_SHAPE.
+ *   - x is [batch][cols] fp32 and y is [batch][rows] fp32, both contiguous. y is
+ *     overwritten, never accumulated into.
+ *   - rows == 0 or n == 0 is a no-op returning QDQ_OK.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream). Launch
+ *     failures return QDQ_ERR_CUDA. A device-side failure (a bounded wait that
+ *     ran out) is recorded in a per-device status word, read back by
+ *     qdq_get_device_status(). Nothing aborts, traps or exits.
+ *   - The caller owns every buffer. Besides plans (below), the library keeps no
+ *     device allocations: only a status word in module memory per device.
+ *   - Calls on different streams may run concurrently. Only sm_103 (GB300)
+ *     devices are accepted; others give QDQ_ERR_DEVICE.
+ */
+#ifndef QDQ_H
+#define QDQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qdq_stream_t; /* == cudaStream_t */
+
+enum qdq_type { QDQ_Q4_0 = 1, QDQ_Q8_0 = 2, QDQ_Q4_K = 3, QDQ_Q6_K = 4 };
+
+enum qdq_status {
+    QDQ_OK = 0,
+    QDQ_ERR_TYPE = -1,     /* unknown block type */
+    QDQ_ERR_SHAPE = -2,    /* negative size, cols or n not a multiple of QK, batch < 1, row too wide */
+    QDQ_ERR_ALIGN = -3,    /* a pointer not 16-byte aligned */
+    QDQ_ERR_PTR = -4,      /* NULL or host pointer */
+    QDQ_ERR_CUDA = -5,     /* a CUDA runtime call or kernel launch failed */
+    QDQ_ERR_TIMEOUT = -6,  /* a device-side bounded wait ran out (from qdq_get_device_status) */
+    QDQ_ERR_DEVICE = -7,   /* current device is not sm_103 */
+    QDQ_ERR_LIMIT = -8     /* more GEMVs or levels than a plan supports */
+};
+
+/* Bytes per block and weights per block of a type; -1 for an unknown type. */
+int qdq_block_bytes(int type);
+int qdq_block_weights(int type);
+
+/* Static text for a status code. */
+const char *qdq_status_string(int status);
+
+/* ---------------------------------------------------------------------------
+ * qdq_dequant: out[i] = w_i for i < n, the fp32 value of each weight.
+ * Cited: "S21 The Capstone: picoLM, in Python", section 2 (dequantize_q4_K:
+ * raw blocks + count n -> n floats); "PicoLM Q6_K quantisation bug"
+ * (dequantize_row_q6_K); "PETIT", What makes it fast & small.
+ * `blocks` holds n/QK consecutive blocks; `out` holds n floats. Each value is
+ * evaluated in the pages' order with IEEE fp32 round-to-nearest and no fused
+ * multiply-add, so the result is bit-for-bit that of a plain CPU decoder.
+ * n must be a multiple of QK (QDQ_ERR_SHAPE).
+ * qdq_dequant runs on the legacy default stream, qdq_dequant_async on `stream`.
+ * ------------------------------------------------------------------------- */
+int qdq_dequant(int type, const void *blocks, int64_t n, float *out_f32);
+int qdq_dequant_async(int type, const void *blocks, int64_t n, float *out_f32,
+                      qdq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * qdq_gemv: y[b][r] = sum_c w[r][c] * x[b][c] for b < batch, r < rows,
+ * with dequantisation fused into the dot product: only the quantised bytes of W
+ * cross the memory bus ("S21 The Capstone: picoLM, in Python", section 3,
+ * fused dequant + dot; picoLM's matmul(out, x, W, n, d, type); PETIT gemv_q8 /
+ * gemv_q4 / gemm).
+ * Accumulation is fp32. Against the exact (double) sum y_ref the result meets
+ * |y - y_ref| <= 1e-5 * sum_c |w[r][c] x[b][c]| + 1e-7 for finite inputs.
+ * batch 1..8 runs the streaming CUDA-core kernel; larger batches the
+ * tensor-core path. Any row width is accepted (wide rows are split into column
+ * chunks inside the kernel).
+ * ------------------------------------------------------------------------- */
+int qdq_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y,
+             int batch, qdq_stream_t stream);
+
+/* One GEMV of a group or plan. */
+typedef struct qdq_gemv_desc {
+    int32_t type;
+    int32_t reserved;
+    const void *W;
+    int64_t rows;
+    int64_t cols;
+    const float *x; /* [batch][cols] */
+    float *y;       /* [batch][rows] */
+} qdq_gemv_desc;
+
+/* Up to 8 independent GEMVs with a common batch, in one launch (for instance
+ * q, k and v of one layer, which may mix Q4_K and Q6_K). Same rules as
+ * qdq_gemv for each; batch must be <= 8. */
+int qdq_gemv_group(const qdq_gemv_desc *descs, int n, int batch, qdq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Plans: a whole decode step's GEMVs in one persistent launch.
+ * ("S21 The Capstone: picoLM, in Python", section 4: model_forward runs, per
+ * layer, the q/k/v, output, gate/up and down projections, then the output head.)
+ * descs[i] belongs to dependency level level[i]; levels must be non-decreasing
+ * from 0. All GEMVs of level k complete (their y written and visible) before any
+ * GEMV of level k+1 reads its x; weight bytes of later levels may be fetched
+ * earlier, since weights never depend on earlier outputs. batch <= 8; at most
+ * 192 GEMVs and 128 levels (QDQ_ERR_LIMIT). The plan copies the descriptors
+ * (not the buffers they point to, which must stay valid while the plan is run)
+ * and allocates one small device array of level counters; destroy frees it.
+ * Runs of one plan must not overlap on the GPU. If qdq_get_device_status()
+ * reports QDQ_ERR_TIMEOUT after a run, call qdq_plan_reset() before the next.
+ * ------------------------------------------------------------------------- */
+typedef struct qdq_plan qdq_plan;
+int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int batch,
+                    qdq_plan **plan_out);
+int qdq_plan_run(qdq_plan *plan, qdq_stream_t stream);
+/* The same run with host I/O: copies x_host (every distinct x buffer of the
+ * plan, concatenated in order of first use, each [batch][cols]) to the plan's x
+ * buffers, runs, and copies every GEMV's y (concatenated in descriptor order)
+ * into y_host. Host buffers should be pinned. Byte counts are returned through
+ * h2d_bytes / d2h_bytes when non-NULL. */
+int qdq_plan_run_io(qdq_plan *plan, const float *x_host, float *y_host, qdq_stream_t stream,
+                    int64_t *h2d_bytes, int64_t *d2h_bytes);
+int qdq_plan_reset(qdq_plan *plan, qdq_stream_t stream);
+void qdq_plan_destroy(qdq_plan *plan);
+/* Number of kernel launches one qdq_plan_run makes (1). */
+int qdq_plan_launches(const qdq_plan *plan);
+
+/* ---------------------------------------------------------------------------
+ * Device status: synchronises `stream`, returns the first device-side error
+ * recorded since the last call (QDQ_OK if none) and clears it.
+ * ------------------------------------------------------------------------- */
+int qdq_get_device_status(qdq_stream_t stream);
+
+/* Runs the library's bounded inter-CTA wait on a device flag that nothing sets,
+ * with a limit of `timeout_ns` nanoseconds, so that a test can see a wait run
+ * out without a hang: afterwards qdq_get_device_status() returns
+ * QDQ_ERR_TIMEOUT. */
+int qdq_selftest_wait_timeout(int64_t timeout_ns, qdq_stream_t stream);
+
+/* Number of streaming multiprocessors the library sizes its grids by. */
+int qdq_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QDQ_H */

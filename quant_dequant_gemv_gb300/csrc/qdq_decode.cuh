@@ -1,0 +1,86 @@
+// qdq_decode.cuh -- block-format field decoders, shared by the standalone
+// dequantisation kernel and the fused GEMV.
+//
+// Layouts:
+//   Q4_K ("S21 The Capstone: picoLM, in Python", section 2): 144 bytes = fp16 d,
+//        fp16 dmin, 12 bytes p[0..11] of 6-bit scale/min fields, 128 nibble bytes
+//        in four 32-byte chunks. Sub-block j (32 weights): j < 4 keeps its scale
+//        in the low six bits of p[j] and its min in the low six bits of p[j+4];
+//        j >= 4 keeps the low four bits of both in p[j+4] (scale low nibble, min
+//        high nibble) and the top two bits in bits 6-7 of p[j-4] (scale) and
+//        p[j] (min). Chunk c holds sub-block 2c in its low nibbles and 2c+1 in
+//        its high nibbles.
+//   Q6_K ("PicoLM Q6_K quantisation bug", block_q6_K): ql[128], qh[64],
+//        int8 scales[16] (one per 16 weights: element e uses scales[e/16]), fp16
+//        d at byte 208. Element e = 128h + 32k + l has low four bits in
+//        ql[64h + 32(k&1) + l] (low nibble for k < 2, high for k >= 2) and top two
+//        bits at bit 2k of qh[32h + l] (the ggml placement); q = q6 - 32.
+//   PETIT q8_0 / q4_0 ("PETIT", How the pieces match): fp32 d + 32 int8, and
+//        fp16 d + 16 bytes whose low nibbles are weights 0-15 and high nibbles
+//        weights 16-31.
+#pragma once
+#include <cstdint>
+
+#include "qdq_device.cuh"
+
+namespace qdq {
+
+// ---- Q4_K -------------------------------------------------------------------------
+// Header words of a Q4_K block: H0 = d | dmin << 16, H1 = p[0..3], H2 = p[4..7],
+// H3 = p[8..11] (little-endian bytes).
+// Returns the 6-bit scales of sub-blocks 2c and 2c+1 in bytes 0 and 1 of *sc and
+// their mins in bytes 0 and 1 of *mn.
+QDQ_DEV void q4k_pair_fields(uint32_t H1, uint32_t H2, uint32_t H3, int c, uint32_t *sc,
+                             uint32_t *mn) {
+    const uint32_t sh = 16u * (uint32_t)(c & 1);
+    if (c < 2) {  // sub-blocks 0..3: six bits in their own byte
+        *sc = (H1 >> sh) & 0x3F3Fu;
+        *mn = (H2 >> sh) & 0x3F3Fu;
+    } else {  // sub-blocks 4..7: low four bits in p[j+4], top two in bits 6-7 of p[j-4] / p[j]
+        const uint32_t lo = H3 >> sh;
+        *sc = (lo & 0x0F0Fu) | (((H1 >> sh) >> 2) & 0x3030u);
+        *mn = ((lo >> 4) & 0x0F0Fu) | (((H2 >> sh) >> 2) & 0x3030u);
+    }
+}
+
+// ---- Q6_K -------------------------------------------------------------------------
+// Given the ql word holding bytes l..l+3 of the run used by k (run k&1) and the qh
+// word holding bytes l..l+3 of qh's half, returns the four 6-bit quants q6 of
+// elements 128h + 32k + l .. +3 as the bytes of one word.
+QDQ_DEV uint32_t q6k_quant_bytes(uint32_t ql, uint32_t qh, int k) {
+    const uint32_t low = (k < 2) ? (ql & 0x0F0F0F0Fu) : ((ql >> 4) & 0x0F0F0F0Fu);
+    uint32_t high;
+    switch (k) {
+        case 0: high = qh << 4; break;
+        case 1: high = qh << 2; break;
+        case 2: high = qh; break;
+        default: high = qh >> 2; break;
+    }
+    return low | (high & 0x30303030u);
+}
+
+// ---- exact per-weight values (for the dequantisation kernel) ---------------------
+// No fused multiply-add: every product and difference is rounded once, in the
+// pages' order.
+QDQ_DEV float q4k_weight(float d, float dmin, uint32_t sc, uint32_t mn, uint32_t q) {
+    return __fsub_rn(__fmul_rn(__fmul_rn(d, (float)sc), (float)q), __fmul_rn(dmin, (float)mn));
+}
+QDQ_DEV float q6k_weight(float d, int sc, int q6) { return __fmul_rn(__fmul_rn(d, (float)sc), (float)(q6 - 32)); }
+QDQ_DEV float q8_0_weight(float d, int q) { return __fmul_rn(d, (float)q); }
+QDQ_DEV float q4_0_weight(float d, int q) { return __fmul_rn((float)(q - 8), d); }
+
+// ---- integer -> float by exponent-field construction (for the fused GEMV) --------
+// For an integer v < 2^23 placed in the low mantissa bits, the float with bits
+// 0x4B000000 | v equals 2^23 + v exactly; subtracting 2^23 (or 2^23 + offset) in
+// fp32 gives v (or v - offset) exactly. A nibble can stay at its bit position p
+// (value q * 2^p) as long as p + 4 <= 23; the matching x is pre-scaled by 2^-p.
+constexpr uint32_t kMagic = 0x4B000000u;
+constexpr float kTwo23 = 8388608.0f;
+
+// One byte of `w` (selector j) as the float 2^23 + byte, in one byte permute.
+template <int J>
+QDQ_DEV uint32_t byte_to_magic(uint32_t w) {
+    return __byte_perm(w, kMagic, (uint32_t)J | 0x7440u);
+}
+
+}  // namespace qdq

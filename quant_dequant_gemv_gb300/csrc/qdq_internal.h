@@ -1,0 +1,43 @@
+// qdq_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qdq.h"
+
+namespace qdq {
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    bool ok = false;
+};
+
+// Cached per device; ok == false when the current device is not sm_103.
+const DeviceInfo &current_device(int *status);
+
+int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStream_t stream, int sm_count);
+
+// The streaming (CUDA-core) GEMV over a list of GEMVs grouped in dependency levels.
+struct StreamPlanHost;  // opaque: the packed kernel arguments
+int stream_plan_build(const qdq_gemv_desc *descs, const int *level, int n, int batch,
+                      unsigned *counters, int sm_count, StreamPlanHost **out);
+int stream_plan_launch(const StreamPlanHost *p, cudaStream_t stream);
+void stream_plan_free(StreamPlanHost *p);
+int stream_plan_nlevels(const StreamPlanHost *p);
+
+int take_status_stream();
+int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);
+
+// The tensor-core batched GEMV (batch >= 9).
+int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y,
+                    int batch, cudaStream_t stream, int sm_count);
+int take_status_mma();
+
+constexpr int kMaxPlanDescs = 192;
+constexpr int kMaxPlanLevels = 128;
+constexpr int kMaxGroupDescs = 8;
+constexpr int kStreamMaxBatch = 8;
+
+}  // namespace qdq

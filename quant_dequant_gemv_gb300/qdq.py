@@ -1,0 +1,182 @@
+"""ctypes binding of libqdq (the C ABI in include/qdq.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels. Buffers may be passed as torch tensors (their data_ptr() is used)
+or as raw integer device addresses. `stream` defaults to torch's current CUDA
+stream. Any non-zero status raises QdqError. If the library is not built or
+cannot be loaded, every call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Sequence
+
+from . import build as _build
+from .synth import Q4_0, Q8_0, Q4_K, Q6_K  # noqa: F401
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+
+
+class QdqError(RuntimeError):
+    def __init__(self, what: str, rc: int):
+        self.rc = rc
+        super().__init__(f"{what}: {status_string(rc)} ({rc})")
+
+
+class GemvDesc(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int32), ("reserved", ctypes.c_int32), ("W", _P), ("rows", _I64),
+                ("cols", _I64), ("x", _P), ("y", _P)]
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqdq.so (built by __graft_entry__.build()). Raises if it is absent."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not path.exists():
+            raise RuntimeError(f"{path} is not built; run __graft_entry__.build() (nvcc, sm_103a)")
+        L = ctypes.CDLL(str(path))
+        sig = {
+            "qdq_block_bytes": (_INT, [_INT]),
+            "qdq_block_weights": (_INT, [_INT]),
+            "qdq_status_string": (ctypes.c_char_p, [_INT]),
+            "qdq_device_sm_count": (_INT, []),
+            "qdq_dequant": (_INT, [_INT, _P, _I64, _P]),
+            "qdq_dequant_async": (_INT, [_INT, _P, _I64, _P, _P]),
+            "qdq_gemv": (_INT, [_INT, _P, _I64, _I64, _P, _P, _INT, _P]),
+            "qdq_gemv_group": (_INT, [ctypes.POINTER(GemvDesc), _INT, _INT, _P]),
+            "qdq_plan_create": (_INT, [ctypes.POINTER(GemvDesc), ctypes.POINTER(_INT), _INT, _INT,
+                                       ctypes.POINTER(_P)]),
+            "qdq_plan_run": (_INT, [_P, _P]),
+            "qdq_plan_run_io": (_INT, [_P, _P, _P, _P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+            "qdq_plan_reset": (_INT, [_P, _P]),
+            "qdq_plan_destroy": (None, [_P]),
+            "qdq_plan_launches": (_INT, [_P]),
+            "qdq_get_device_status": (_INT, [_P]),
+            "qdq_selftest_wait_timeout": (_INT, [_I64, _P]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+# Every name the header declares (the C ABI's exported symbols).
+EXPORTS = ["qdq_block_bytes", "qdq_block_weights", "qdq_status_string", "qdq_device_sm_count",
+           "qdq_dequant", "qdq_dequant_async", "qdq_gemv", "qdq_gemv_group", "qdq_plan_create",
+           "qdq_plan_run", "qdq_plan_run_io", "qdq_plan_reset", "qdq_plan_destroy",
+           "qdq_plan_launches", "qdq_get_device_status", "qdq_selftest_wait_timeout"]
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != 0:
+        raise QdqError(what, rc)
+
+
+def status_string(rc: int) -> str:
+    return lib().qdq_status_string(rc).decode()
+
+
+def block_bytes(qtype: int) -> int:
+    return lib().qdq_block_bytes(qtype)
+
+
+def block_weights(qtype: int) -> int:
+    return lib().qdq_block_weights(qtype)
+
+
+def device_sm_count() -> int:
+    n = lib().qdq_device_sm_count()
+    if n < 0:
+        raise QdqError("qdq_device_sm_count", n)
+    return n
+
+
+def dequant(qtype: int, blocks, n: int, out, stream=None) -> None:
+    _check(lib().qdq_dequant_async(qtype, _ptr(blocks), n, _ptr(out), _stream(stream)), "qdq_dequant")
+
+
+def gemv(qtype: int, W, rows: int, cols: int, x, y, batch: int = 1, stream=None) -> None:
+    _check(lib().qdq_gemv(qtype, _ptr(W), rows, cols, _ptr(x), _ptr(y), batch, _stream(stream)), "qdq_gemv")
+
+
+def _descs(items: Sequence[tuple]) -> ctypes.Array:
+    arr = (GemvDesc * max(len(items), 1))()
+    for i, (qtype, W, rows, cols, x, y) in enumerate(items):
+        arr[i] = GemvDesc(qtype, 0, _ptr(W), rows, cols, _ptr(x), _ptr(y))
+    return arr
+
+
+def gemv_group(items: Sequence[tuple], batch: int = 1, stream=None) -> None:
+    """items: (type, W, rows, cols, x, y) for each GEMV."""
+    _check(lib().qdq_gemv_group(_descs(items), len(items), batch, _stream(stream)), "qdq_gemv_group")
+
+
+class Plan:
+    """A decode step's GEMVs in dependency levels, run as one persistent launch."""
+
+    def __init__(self, items: Sequence[tuple], levels: Sequence[int], batch: int = 1):
+        self._keep = items  # the caller's buffers must outlive the plan
+        self.batch = batch
+        lv = (_INT * len(levels))(*levels)
+        h = _P()
+        _check(lib().qdq_plan_create(_descs(items), lv, len(items), batch, ctypes.byref(h)), "qdq_plan_create")
+        self._h = h
+
+    def run(self, stream=None) -> None:
+        _check(lib().qdq_plan_run(self._h, _stream(stream)), "qdq_plan_run")
+
+    def run_io(self, x_host, y_host, stream=None) -> tuple[int, int]:
+        hb, db = _I64(), _I64()
+        _check(lib().qdq_plan_run_io(self._h, _ptr(x_host), _ptr(y_host), _stream(stream), ctypes.byref(hb),
+                                     ctypes.byref(db)), "qdq_plan_run_io")
+        return hb.value, db.value
+
+    def reset(self, stream=None) -> None:
+        _check(lib().qdq_plan_reset(self._h, _stream(stream)), "qdq_plan_reset")
+
+    @property
+    def launches(self) -> int:
+        return lib().qdq_plan_launches(self._h)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().qdq_plan_destroy(self._h)
+            self._h = _P()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def get_device_status(stream=None) -> int:
+    return lib().qdq_get_device_status(_stream(stream))
+
+
+def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
+    _check(lib().qdq_selftest_wait_timeout(timeout_ns, _stream(stream)), "qdq_selftest_wait_timeout")
