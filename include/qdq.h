@@ -147,6 +147,25 @@ void qdq_plan_destroy(qdq_plan *plan);
 int qdq_plan_launches(const qdq_plan *plan);
 
 /* ---------------------------------------------------------------------------
+ * qdq_gemv_levels_noalloc: the same computation as a plan built from (descs,
+ * level, n, batch) and run once, for callers that cannot allocate device
+ * memory (a host framework that owns the whole memory budget, a serving loop
+ * that must not call the allocator, a process whose allocations all go through
+ * another component). It calls no cudaMalloc or other allocating routine: the
+ * level counters live in a 512-byte array in the library's module memory,
+ * which every GPU that loads the library keeps until exit. No counterpart on
+ * the pages: this is a deployment variant of the plan launch.
+ * Limits: at most 128 levels (QDQ_ERR_LIMIT), 192 GEMVs, batch <= 8.
+ * The array is shared by every call; each call clears the counters it uses on
+ * `stream` first. Calls whose kernels overlap on the GPU race on the array, so
+ * serialise them (one stream, or events). The first call on a device looks up
+ * the array's device address with that device current; make that first call
+ * before any stream capture.
+ * ------------------------------------------------------------------------- */
+int qdq_gemv_levels_noalloc(const qdq_gemv_desc *descs, const int *level, int n, int batch,
+                            qdq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Device status: synchronises `stream`, returns the first device-side error
  * recorded since the last call (QDQ_OK if none) and clears it.
  * ------------------------------------------------------------------------- */

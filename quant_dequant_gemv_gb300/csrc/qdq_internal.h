@@ -26,6 +26,8 @@ int stream_plan_build(const qdq_gemv_desc *descs, const int *level, int n, int b
 int stream_plan_launch(const StreamPlanHost *p, cudaStream_t stream);
 void stream_plan_free(StreamPlanHost *p);
 int stream_plan_nlevels(const StreamPlanHost *p);
+int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, int n, int batch,
+                                 unsigned *counters, int sm_count, cudaStream_t stream);
 
 int take_status_stream();
 int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);

@@ -1,0 +1,93 @@
+// qdq_noalloc.cu -- the dependency-level GEMV launch for callers that cannot
+// allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code that runs inside a fixed memory
+// budget handed to it by a host framework, code that must not touch the
+// allocator once a serving loop is running, or code linked into a process whose
+// allocations all go through another component. qdq_plan_create allocates the
+// plan's level counters with cudaMalloc; qdq_gemv_levels_noalloc runs the same
+// persistent kernel with its counters in a file-scope device array instead.
+//
+// The array holds kNoAllocMaxLevels counters (512 bytes). Every GPU that loads
+// the library keeps it until the process exits, and every call shares it: the
+// call clears the counters it uses on `stream` before the launch, and two calls
+// whose kernels overlap on the GPU race on the array.
+#include <mutex>
+
+#include "qdq_internal.h"
+
+namespace qdq {
+
+constexpr int kNoAllocMaxLevels = 128;
+
+static __device__ __align__(256) unsigned s_noalloc_level_counters[kNoAllocMaxLevels];
+
+// Device address of the array, looked up once per device with that device current.
+static unsigned *s_counters_addr[64];
+static std::mutex s_counters_mu;
+
+static int counters_for_device(int device, unsigned **out) {
+    std::lock_guard<std::mutex> lock(s_counters_mu);
+    if (s_counters_addr[device] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, s_noalloc_level_counters) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return QDQ_ERR_CUDA;
+        }
+        s_counters_addr[device] = (unsigned *)p;
+    }
+    *out = s_counters_addr[device];
+    return QDQ_OK;
+}
+
+static int check_ptr(const void *p, int device) {
+    if (p == nullptr) return QDQ_ERR_PTR;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return QDQ_ERR_PTR;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return QDQ_ERR_PTR;
+    if (attr.type == cudaMemoryTypeDevice && attr.device != device) return QDQ_ERR_PTR;
+    return ((uintptr_t)p & 15) ? QDQ_ERR_ALIGN : QDQ_OK;
+}
+
+}  // namespace qdq
+
+using namespace qdq;
+
+extern "C" int qdq_gemv_levels_noalloc(const qdq_gemv_desc *descs, const int *level, int n, int batch,
+                                       qdq_stream_t stream) {
+    if (descs == nullptr || level == nullptr) return QDQ_ERR_PTR;
+    if (n < 1 || n > kMaxPlanDescs) return QDQ_ERR_LIMIT;
+    if (batch < 1) return QDQ_ERR_SHAPE;
+    if (batch > kStreamMaxBatch) return QDQ_ERR_LIMIT;
+    if (level[0] != 0) return QDQ_ERR_SHAPE;
+    for (int i = 1; i < n; ++i)
+        if (level[i] != level[i - 1] && level[i] != level[i - 1] + 1) return QDQ_ERR_SHAPE;
+    const int nlevels = level[n - 1] + 1;
+    if (nlevels > kNoAllocMaxLevels) return QDQ_ERR_LIMIT;
+    int rc;
+    const DeviceInfo &dev = current_device(&rc);
+    if (rc) return rc;
+    for (int i = 0; i < n; ++i) {
+        const qdq_gemv_desc &d = descs[i];
+        const int qk = qdq_block_weights(d.type);
+        if (qk < 0) return QDQ_ERR_TYPE;
+        if (d.rows < 1 || d.cols < 1 || d.cols % qk || d.rows > ((int64_t)1 << 40) || d.cols > ((int64_t)1 << 30))
+            return QDQ_ERR_SHAPE;
+        if ((rc = check_ptr(d.W, dev.device)) || (rc = check_ptr(d.x, dev.device)) ||
+            (rc = check_ptr(d.y, dev.device)))
+            return rc;
+        for (int k = 0; k < i; ++k)
+            if (descs[k].x == d.x && descs[k].cols != d.cols) return QDQ_ERR_SHAPE;
+    }
+    unsigned *counters = nullptr;
+    if ((rc = counters_for_device(dev.device, &counters))) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(counters, 0, sizeof(unsigned) * nlevels, s) != cudaSuccess) {
+        cudaGetLastError();
+        return QDQ_ERR_CUDA;
+    }
+    return stream_launch_levels_inplace(descs, level, n, batch, counters, dev.sm_count, s);
+}

@@ -885,6 +885,23 @@ int stream_plan_launch(const StreamPlanHost *p, cudaStream_t stream) {
     }
 }
 
+// Multi-level launch with caller-provided level counters and no heap use: the
+// kernel arguments live on this function's stack (about 10 KiB).
+int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, int n, int batch,
+                                 unsigned *counters, int sm_count, cudaStream_t stream) {
+    using A = StreamArgs<kMaxPlanDescs, kMaxPlanLevels>;
+    A args;
+    StreamPlanHost p;
+    p.bt = bt_of(batch);
+    p.grid = sm_count;
+    p.big = true;
+    p.cooperative = true;
+    p.args = &args;
+    p.args_bytes = sizeof(A);
+    fill_args(&args, descs, level, n, batch, counters, p.bt);
+    return stream_plan_launch(&p, stream);
+}
+
 void stream_plan_free(StreamPlanHost *p) {
     if (!p) return;
     free(p->args);

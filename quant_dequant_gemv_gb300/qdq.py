@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
             "qdq_plan_launches": (_INT, [_P]),
             "qdq_get_device_status": (_INT, [_P]),
             "qdq_selftest_wait_timeout": (_INT, [_I64, _P]),
+            "qdq_gemv_levels_noalloc": (_INT, [ctypes.POINTER(GemvDesc), ctypes.POINTER(_INT), _INT, _INT, _P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -71,7 +72,8 @@ def lib() -> ctypes.CDLL:
 EXPORTS = ["qdq_block_bytes", "qdq_block_weights", "qdq_status_string", "qdq_device_sm_count",
            "qdq_dequant", "qdq_dequant_async", "qdq_gemv", "qdq_gemv_group", "qdq_plan_create",
            "qdq_plan_run", "qdq_plan_run_io", "qdq_plan_reset", "qdq_plan_destroy",
-           "qdq_plan_launches", "qdq_get_device_status", "qdq_selftest_wait_timeout"]
+           "qdq_plan_launches", "qdq_get_device_status", "qdq_selftest_wait_timeout",
+           "qdq_gemv_levels_noalloc"]
 
 
 def _ptr(t) -> int:
@@ -172,6 +174,14 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+def gemv_levels_noalloc(items: Sequence[tuple], levels: Sequence[int], batch: int = 1, stream=None) -> None:
+    """The plan computation in one call that allocates no device memory (its
+    level counters live in a fixed 512-byte array inside the library)."""
+    lv = (_INT * len(levels))(*levels)
+    _check(lib().qdq_gemv_levels_noalloc(_descs(items), lv, len(items), batch, _stream(stream)),
+           "qdq_gemv_levels_noalloc")
 
 
 def get_device_status(stream=None) -> int:
