@@ -32,15 +32,14 @@ namespace qdq {
 // their mins in bytes 0 and 1 of *mn.
 QDQ_DEV void q4k_pair_fields(uint32_t H1, uint32_t H2, uint32_t H3, int c, uint32_t *sc,
                              uint32_t *mn) {
+    // Branch-free over c, so the four chunk lanes of a super-block do not diverge.
     const uint32_t sh = 16u * (uint32_t)(c & 1);
-    if (c < 2) {  // sub-blocks 0..3: six bits in their own byte
-        *sc = (H1 >> sh) & 0x3F3Fu;
-        *mn = (H2 >> sh) & 0x3F3Fu;
-    } else {  // sub-blocks 4..7: low four bits in p[j+4], top two in bits 6-7 of p[j-4] / p[j]
-        const uint32_t lo = H3 >> sh;
-        *sc = (lo & 0x0F0Fu) | (((H1 >> sh) >> 2) & 0x3030u);
-        *mn = ((lo >> 4) & 0x0F0Fu) | (((H2 >> sh) >> 2) & 0x3030u);
-    }
+    const uint32_t upper = (uint32_t)(c >> 1);  // 0: sub-blocks 0..3, 1: sub-blocks 4..7
+    const uint32_t top = 2u * upper;            // the top two bits sit at bits 4-5 or 6-7
+    const uint32_t a = (upper ? H3 : H1) >> sh;
+    const uint32_t b = (upper ? (H3 >> 4) : H2) >> sh;
+    *sc = (a & 0x0F0Fu) | (((H1 >> sh) >> top) & 0x3030u);
+    *mn = (b & 0x0F0Fu) | (((H2 >> sh) >> top) & 0x3030u);
 }
 
 // ---- Q6_K -------------------------------------------------------------------------
