@@ -82,4 +82,61 @@ QDQ_DEV uint32_t byte_to_magic(uint32_t w) {
     return __byte_perm(w, kMagic, (uint32_t)J | 0x7440u);
 }
 
+
+// ---- four consecutive weights of one block, exactly (shared by the standalone
+// dequantisation kernel and the tensor-core path) -------------------------------
+QDQ_DEV uint32_t ldg_u16(const uint8_t *p) { return (uint32_t)__ldg((const unsigned short *)p); }
+QDQ_DEV uint32_t ldg_u32(const uint8_t *p) { return __ldg((const unsigned int *)p); }
+// 4 bytes at a 2-byte-aligned address
+QDQ_DEV uint32_t ldg_u32_a2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p + 2) << 16); }
+
+// Weights e0 .. e0+3 (e0 a multiple of 4) of the block at `blk`.
+template <int TYPE>
+QDQ_DEV float4 decode4(const uint8_t *blk, int e0) {
+    float4 v;
+    if constexpr (TYPE == QDQ_Q4_K) {  // blk 16-byte aligned
+        const uint4 H = __ldg((const uint4 *)blk);
+        const int c = e0 >> 6, i = e0 & 63;
+        const bool high = i >= 32;
+        uint32_t sc2, mn2;
+        q4k_pair_fields(H.y, H.z, H.w, c, &sc2, &mn2);
+        const uint32_t sc = high ? (sc2 >> 8) : (sc2 & 0xFF);
+        const uint32_t mn = high ? (mn2 >> 8) : (mn2 & 0xFF);
+        const float d = half_bits_to_float(H.x & 0xFFFF), dmin = half_bits_to_float(H.x >> 16);
+        uint32_t q = ldg_u32(blk + 16 + 32 * c + (i & 31));
+        if (high) q >>= 4;
+        v.x = q4k_weight(d, dmin, sc, mn, q & 15);
+        v.y = q4k_weight(d, dmin, sc, mn, (q >> 8) & 15);
+        v.z = q4k_weight(d, dmin, sc, mn, (q >> 16) & 15);
+        v.w = q4k_weight(d, dmin, sc, mn, (q >> 24) & 15);
+    } else if constexpr (TYPE == QDQ_Q6_K) {  // blk 2-byte aligned
+        const int h = e0 >> 7, k = (e0 >> 5) & 3, l = e0 & 31;
+        const uint32_t ql = ldg_u32_a2(blk + 64 * h + 32 * (k & 1) + l);
+        const uint32_t qh = ldg_u32_a2(blk + 128 + 32 * h + l);
+        const int sc = (int)(int8_t)__ldg(blk + 192 + (e0 >> 4));
+        const float d = half_bits_to_float(ldg_u16(blk + 208));
+        const uint32_t q6 = q6k_quant_bytes(ql, qh, k);
+        v.x = q6k_weight(d, sc, (int)(q6 & 0xFF));
+        v.y = q6k_weight(d, sc, (int)((q6 >> 8) & 0xFF));
+        v.z = q6k_weight(d, sc, (int)((q6 >> 16) & 0xFF));
+        v.w = q6k_weight(d, sc, (int)(q6 >> 24));
+    } else if constexpr (TYPE == QDQ_Q8_0) {  // blk 4-byte aligned
+        const float d = __uint_as_float(ldg_u32(blk));
+        const uint32_t q = ldg_u32(blk + 4 + e0);
+        v.x = q8_0_weight(d, (int)(int8_t)(q & 0xFF));
+        v.y = q8_0_weight(d, (int)(int8_t)((q >> 8) & 0xFF));
+        v.z = q8_0_weight(d, (int)(int8_t)((q >> 16) & 0xFF));
+        v.w = q8_0_weight(d, (int)(int8_t)(q >> 24));
+    } else {  // QDQ_Q4_0, blk 2-byte aligned
+        const float d = half_bits_to_float(ldg_u16(blk));
+        uint32_t q = ldg_u32_a2(blk + 2 + (e0 & 15));
+        if (e0 >= 16) q >>= 4;
+        v.x = q4_0_weight(d, (int)(q & 15));
+        v.y = q4_0_weight(d, (int)((q >> 8) & 15));
+        v.z = q4_0_weight(d, (int)((q >> 16) & 15));
+        v.w = q4_0_weight(d, (int)((q >> 24) & 15));
+    }
+    return v;
+}
+
 }  // namespace qdq

@@ -55,13 +55,14 @@ static __device__ int s_status_stream;
 
 constexpr int kConsumerWarps = 8;
 constexpr int kFirstConsumerWarp = 2;
+constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + kFirstConsumerWarp);
 constexpr int kStageBytes = 32768;
 constexpr int kCB = 2048;  // columns per column block (32 lanes x 64)
 
 template <int BT> struct Cfg;
 // kStages: ring depth; kXBytes / kXSumBytes: one x slot (there are two)
-template <> struct Cfg<1> { static constexpr int kStages = 4, kXBytes = 45056, kXSumBytes = 1024; };
+template <> struct Cfg<1> { static constexpr int kStages = 5, kXBytes = 24576, kXSumBytes = 1024; };
 template <> struct Cfg<2> { static constexpr int kStages = 4, kXBytes = 40960, kXSumBytes = 2048; };
 template <> struct Cfg<4> { static constexpr int kStages = 4, kXBytes = 40960, kXSumBytes = 2048; };
 template <> struct Cfg<8> { static constexpr int kStages = 4, kXBytes = 40960, kXSumBytes = 2048; };
@@ -91,7 +92,7 @@ struct StreamArgs {
 template <int BT, int MAXD>
 constexpr int smem_bytes() {
     return Cfg<BT>::kStages * kStageBytes + 2 * Cfg<BT>::kXBytes + 2 * Cfg<BT>::kXSumBytes + MAXD * 16 +
-           (2 * Cfg<BT>::kStages + 7) * 8;
+           (2 * Cfg<BT>::kStages + 6) * 8;
 }
 
 // ---------------------------------------------------------------------------
@@ -103,11 +104,10 @@ __host__ __device__ constexpr int blk_bytes(int t) {
 __host__ __device__ constexpr int blk_weights(int t) { return (t == QDQ_Q4_K || t == QDQ_Q6_K) ? 256 : 32; }
 __host__ __device__ constexpr int x_kind(int t) { return t == QDQ_Q4_K ? 1 : t == QDQ_Q4_0 ? 2 : 0; }
 
-// Float offsets inside an x slot: first the landing area of the bulk copy
-// (x as it is in global memory), then the swizzled copies in kind order; each
-// region is [batch][kc] floats.
+// Float offsets inside an x slot: the swizzled copies in kind order, each
+// [batch][kc] floats.
 QDQ_DEV int copy_offset(int kinds, int kind, int kc, int BT) {
-    int off = kc * BT;
+    int off = 0;
     for (int k = 0; k < kind; ++k)
         if ((kinds >> k) & 1) off += kc * BT;
     return off;
@@ -663,8 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = (uint64_t *)(ranges + 2 * MAXD);
     const uint32_t ring_a = smem_u32(ring), xslot_a = smem_u32(xslot), xsum_a = smem_u32(xsum);
     const uint32_t full_a = smem_u32(bars), empty_a = full_a + 8 * NST;
-    const uint32_t xfull_a = empty_a + 8 * NST, xempty_a = xfull_a + 16, lvl_a = xempty_a + 16;
-    const uint32_t xload_a = lvl_a + 8;  // two barriers: raw x landed in a slot
+    // xready[2]: x slot staged (8 warp arrivals); xempty[2]: slot no longer read;
+    // lvl: this CTA's consumers finished a level; dep: all CTAs finished the
+    // previous level (arrival by the control warp).
+    const uint32_t xready_a = empty_a + 8 * NST, xempty_a = xready_a + 16, lvl_a = xempty_a + 16;
+    const uint32_t dep_a = lvl_a + 8;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x, P = gridDim.x;
@@ -678,12 +681,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty_a + 8 * s, kConsumerWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(xfull_a + 8 * b, 1);
+            mbar_init(xready_a + 8 * b, kConsumerWarps);
             mbar_init(xempty_a + 8 * b, kConsumerWarps);
         }
         mbar_init(lvl_a, kConsumerWarps);
-        mbar_init(xload_a, 1);
-        mbar_init(xload_a + 8, 1);
+        mbar_init(dep_a, 1);
         fence_mbar_init();
     }
     // this CTA's row range of every GEMV
@@ -716,81 +718,98 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 1) {
         // ------------------------------------------------------------ control
-        // This CTA has finished level L. The level-done barrier completes one phase
-        // per level in which this CTA had tiles (consumers arrive only then), so
-        // consumers can never be two phases ahead: they need the next level's x,
-        // which is staged only after this wait.
-        int lvl_phase = 0;
-        bool had_tiles = false;
-        int xload_uses[2] = {0, 0};
-        int cur_level = 0;
-        (void)cur_level;
-        auto publish_level = [&](int L) {
-            if (had_tiles) mbar_wait(lvl_a, (lvl_phase++) & 1, status);
-            had_tiles = false;
-            if (lane == 0) {
-                // Consumers' y stores are ordered before their arrivals on the level
-                // barrier (CTA scope); the release below makes them visible at GPU
-                // scope together with the count.
-                if (L < a.nlevels - 1) {
-                    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&a.counters[L]) : "memory");
-                } else {
-                    __threadfence();
-                    const unsigned old = atomicAdd(&a.counters[L], 1u);
-                    if (old == (unsigned)P - 1) {
-                        // every CTA has passed every wait: reset for the next run
-                        for (int i = 0; i < a.nlevels; ++i) a.counters[i] = 0u;
-                        __threadfence();
-                    }
-                }
-            }
+        // Publishes level L once this CTA's consumers have finished it, then
+        // waits until every CTA has, and releases the consumers into level L+1.
+        // The level barrier completes one phase per level in which this CTA has
+        // tiles (consumers arrive only then) and so does dep (arrived only for
+        // levels with tiles): neither can run two phases ahead of its waiter,
+        // since consumers reach a level's work only through dep and dep for a
+        // later level needs this level's publication first.
+        if (!levels_synced) return;
+        auto has_tiles = [&](int L) {
+            for (int g = a.level_start[L]; g < a.level_start[L + 1]; ++g)
+                if (ranges[2 * g] < ranges[2 * g + 1]) return true;
+            return false;
         };
-        walk(
-            a, ranges,
-            [&](int L) {
-                if (lane == 0) QDQ_TR(L, 0);
-                if (L > 0 && levels_synced) {
-                    publish_level(L - 1);
-                    if (lane == 0) QDQ_TR(L, 1);
-                    if (lane == 0) wait_counter(&a.counters[L - 1], (unsigned)P, status, kWaitLimitNs);
-                    if (lane == 0) QDQ_TR(L, 2);
+        int lvl_phase = 0;
+        bool prev_had = has_tiles(0);
+        for (int L = 1; L < a.nlevels; ++L) {
+            if (lane == 0) QDQ_TR(L, 0);
+            if (prev_had) mbar_wait(lvl_a, (lvl_phase++) & 1, status);
+            if (lane == 0) {
+                QDQ_TR(L, 1);
+                // Consumers' y stores are ordered before their arrivals on the level
+                // barrier (CTA scope); the release makes them visible at GPU scope
+                // together with the count.
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&a.counters[L - 1]) : "memory");
+                wait_counter(&a.counters[L - 1], (unsigned)P, status, kWaitLimitNs);
+                QDQ_TR(L, 2);
+            }
+            __syncwarp();
+            const bool had = has_tiles(L);
+            if (had && lane == 0) mbar_arrive(dep_a);
+            prev_had = had;
+        }
+        if (prev_had) mbar_wait(lvl_a, (lvl_phase++) & 1, status);
+        if (lane == 0) {
+            __threadfence();
+            const unsigned old = atomicAdd(&a.counters[a.nlevels - 1], 1u);
+            if (old == (unsigned)P - 1) {
+                // every CTA has passed every wait: reset for the next run
+                for (int i = 0; i < a.nlevels; ++i) a.counters[i] = 0u;
+                __threadfence();
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp - kFirstConsumerWarp;
+    const int ctid = (int)threadIdx.x - 32 * kFirstConsumerWarp;
+    int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0, dep_phase = 0;
+    bool had_tiles = false, dep_pending = false;
+    (void)cur_level;
+    (void)tiles_in_level;
+    XSlice xr;
+    int xr_key = -1;  // (epoch, column block, format) of the x values in xr
+
+    walk(
+        a, ranges,
+        [&](int L) {
+            cur_level = L;
+            tiles_in_level = 0;
+            dep_pending = L > 0 && levels_synced;
+        },
+        [&](const Tile &tl, const TileGeom &geo, int e, bool, const DevDesc &d) {
+            had_tiles = true;
+            if (cw == 0 && lane == 0 && tiles_in_level == 0) QDQ_TR(cur_level, 4);
+            if (e != cur_e) {
+                if (cur_e >= 0) {
                     __syncwarp();
+                    if (lane == 0) mbar_arrive(xempty_a + 8 * (cur_e & 1));
                 }
-                cur_level = L;
-            },
-            [&](const Tile &tl, const TileGeom &, int e, bool fresh, const DevDesc &d) {
-                had_tiles = true;
-                if (!fresh) return;
+                if (dep_pending) {  // the previous level is complete on every CTA
+                    mbar_wait(dep_a, (dep_phase++) & 1, status);
+                    dep_pending = false;
+                }
+                cur_e = e;
                 const int b = e & 1;
                 if (e >= 2) mbar_wait(xempty_a + 8 * b, ((e >> 1) - 1) & 1, status);
-                // Stage x[:, kc0 : kc0 + kcols] into slot b: one bulk copy per batch
-                // row into the landing area, then the swizzled copies (plain and/or
-                // pre-scaled for the nibble formats) and the Q4_K sub-block sums.
-                const uint32_t land_a = xslot_a + b * XB;
-                float *xs = (float *)(xslot + b * XB);  // landing area at offset 0
+                // Stage x[:, kc0 : kc0 + kcols] into slot b (every consumer thread a
+                // share): swizzled plain and/or pre-scaled copies, and the Q4_K
+                // sub-block sums of x. Loads bypass L1: x may have been written by
+                // other SMs during this kernel.
+                float *xs = (float *)(xslot + b * XB);
                 float *xsm = (float *)(xsum + b * XSB);
                 const int kc = tl.kcols, n4 = kc / 4;
                 const bool k0 = d.kinds & 1, k1 = d.kinds & 2, k2 = d.kinds & 4;
-                const uint32_t bar = xload_a + 8 * b;
-                for (int i = batch * n4 + lane; i < BT * n4; i += 32)  // padded batch rows are zero
-                    ((float4 *)xs)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                __syncwarp();
-                if (lane == 0) {
-                    // order earlier generic writes of x (for instance y of an earlier
-                    // level) before the bulk copy's reads
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    mbar_arrive_expect_tx(bar, (uint32_t)(batch * kc * 4));
-                    for (int bb = 0; bb < batch; ++bb)
-                        bulk_g2s(land_a + (uint32_t)(bb * kc * 4), d.x + (int64_t)bb * d.cols + tl.kc0,
-                                 (uint32_t)(kc * 4), bar);
-                }
-                mbar_wait(bar, (xload_uses[b]++) & 1, status);
                 const int o0 = copy_offset(d.kinds, 0, kc, BT), o1 = copy_offset(d.kinds, 1, kc, BT),
                           o2 = copy_offset(d.kinds, 2, kc, BT);
 #pragma unroll 4
-                for (int i = lane; i < n4 * BT; i += 32) {
+                for (int i = ctid; i < n4 * BT; i += kConsumers) {
                     const int bb = i / n4, c = i - bb * n4, col = 4 * c;
-                    const float4 v = ((const float4 *)xs)[i];
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (bb < batch) v = __ldcg((const float4 *)(d.x + (int64_t)bb * d.cols + tl.kc0) + c);
                     const int at = bb * kc + 4 * xswz(c);
                     if (k0) *(float4 *)(xs + o0 + at) = v;
                     if (k1) {  // Q4_K: low nibbles are columns 0..31 of each 64
@@ -813,39 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(xfull_a + 8 * b);
-                if (lane == 0) QDQ_TR(cur_level, 3);
-            },
-            [](int) {});
-        if (levels_synced) publish_level(a.nlevels - 1);
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    const int cw = warp - kFirstConsumerWarp;
-    int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0;
-    bool had_tiles = false;
-    (void)cur_level;
-    (void)tiles_in_level;
-    XSlice xr;
-    int xr_key = -1;  // (epoch, column block, format) of the x values in xr
-
-    walk(
-        a, ranges,
-        [&](int L) {
-            cur_level = L;
-            tiles_in_level = 0;
-        },
-        [&](const Tile &tl, const TileGeom &geo, int e, bool, const DevDesc &d) {
-            had_tiles = true;
-            if (cw == 0 && lane == 0 && tiles_in_level == 0) QDQ_TR(cur_level, 4);
-            if (e != cur_e) {
-                if (cur_e >= 0) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xempty_a + 8 * (cur_e & 1));
-                }
-                cur_e = e;
-                mbar_wait(xfull_a + 8 * (e & 1), (e >> 1) & 1, status);
+                if (lane == 0) mbar_arrive(xready_a + 8 * b);
+                mbar_wait(xready_a + 8 * b, (e >> 1) & 1, status);
             }
             if (cw == 0 && lane == 0 && tiles_in_level == 0) QDQ_TR(cur_level, 5);
             const int s = t % NST;
@@ -943,6 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(lvl_a);  // release (CTA scope) of this warp's y stores
             }
             had_tiles = false;
+            dep_pending = false;  // a level without tiles here needs no release
         });
 }
 
@@ -1008,7 +997,7 @@ static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, con
     }
     for (int i = 0; i < n; ++i) {
         DevDesc &d = A->d[i];
-        const int nregions = 1 + __builtin_popcount(d.kinds);  // landing area + swizzled copies
+        const int nregions = __builtin_popcount(d.kinds);  // swizzled copies
         int kc_x = xbytes_of(BT) / (4 * BT * nregions);
         const int kc_s = (xsumbytes_of(BT) / (4 * BT)) * 32;  // Q4_K sums fit their slot
         if (kc_s < kc_x) kc_x = kc_s;
