@@ -1,33 +1,34 @@
 // qdq_mma.cu -- batched dequant-GEMV on the 5th-generation tensor cores (tcgen05).
 //
-// y[b][r] = sum_c w[r][c] x[b][c] is computed as D = W X^T: W is the A operand
-// (M = 128 rows per tile, K-major, in tensor memory), X the B operand (N = batch,
-// K-major, in shared memory), and D is accumulated in fp32 in tensor memory. A
-// bf16 operand keeps 8 significant bits, too few for the GEMV tolerance
-// 1e-5 * sum|w x|, so both sides are split into two bf16 terms, w = w_hi + w_lo
-// and x = x_hi + x_lo with w_hi = bf16(w) and w_lo = bf16(w - w_hi) (round to
-// nearest), and w x is taken as w_hi x_hi + w_hi x_lo + w_lo x_hi (the "bf16x3"
-// product of Henry, Tang and Heinecke, "Leveraging the bfloat16 Artificial
-// Intelligence Datatype For Higher-Precision Computations", ARITH 2019). Each
-// term dropped or rounded away is below 2^-16 |w x|. The first two products are
-// one MMA with N = 2 b_pad against B = [x_hi; x_lo]; the third is one MMA with
-// N = b_pad against x_hi.
+// y[b][r] = sum_c w[r][c] x[b][c] with w = s_g q (+ m_g for Q4_K) inside each scale
+// group g of a row (32 weights for Q4_K sub-blocks, q8_0 and q4_0 blocks; 16 for
+// Q6_K). Per group the kernel forms Z_g[r][b] = sum_{c in g} q[r][c] x[b][c] on the
+// tensor cores and applies the scales on the CUDA cores:
+//     y[b][r] = sum_g ( s_g Z_g[r][b] - m_g X_g[b] ),  X_g[b] = sum_{c in g} x[b][c]
+// (Q4_K: s = d sc, m = dmin mn; Q6_K: s = d sc, m = 0; q8_0 / q4_0: s = d, m = 0).
+// The quants q are small integers, so the A operand (W, M = 128 rows per tile, in
+// tensor memory) holds them exactly in bf16; x is split into two bf16 terms,
+// x = x_hi + x_lo (round to nearest each), so every product is exact up to the
+// rounding of x_lo: |error| <= 2^-17 |w x|, inside the GEMV tolerance for any
+// input. Z_g accumulates q x_hi + q x_lo in fp32 tensor memory (two MMAs with
+// N = b_pad), one accumulator region per group.
 //
 // X is split once per call by a small kernel into a scratch buffer already in
-// the MMA's canonical K-major layout, so every CTA copies its B tiles with one
-// bulk copy per 64 columns.
+// the MMA's canonical K-major layout (and, for Q4_K, the group sums X_g), so
+// every CTA copies its B tiles with one bulk copy per 64 columns.
 //
 // One CTA per SM, 19 warps:
 //   warp 0      copies the raw blocks of 128 rows x 256 weights into a ring, with
 //               2-D tensor copies of W viewed as [rows / g][g row_bytes]
 //               (L2 evict-first);
-//   warp 1      owns the tensor memory; its lane 0 issues the MMAs and commits;
+//   warp 1      owns the tensor memory; its elected lane issues the MMAs;
 //   warp 2      copies the split X of each 64-column sub-chunk into a ring;
-//   warps 3-18  decode: thread (row, run) turns a run of 16 consecutive weights
-//               of its row per sub-chunk into fp32 with the pages' formulas,
-//               splits them and stores the A operand to tensor memory
-//               (tcgen05.st). Four warps per row quarter hide each other's
-//               latencies.
+//   warps 3-18  thread (row, run) turns a run of 16 consecutive quants of its row
+//               per sub-chunk into exact bf16 (a byte permute puts each quant
+//               under the bf16 exponent of 128, a bf16 subtraction removes the
+//               offset) and stores them to tensor memory; two sub-chunks later
+//               the same thread reads its group's accumulator back and adds
+//               s_g Z_g (- m_g X_g) into registers.
 // Split-K: the CTAs that share a row tile form a thread-block cluster along K.
 // Each leaves its partial tile in shared memory and the cluster sums the
 // partials through distributed shared memory in rank order, so y is
@@ -64,7 +65,16 @@ __device__ unsigned long long *g_mma_trace;
             g_mma_trace[((size_t)(blockIdx.y * gridDim.x + blockIdx.x) * 8 + (slot)) * 64 + (idx)] = \
                 globaltimer_ns();                                                                    \
     } while (0)
+#define MTC(slot, idx)                                                                               \
+    do {                                                                                             \
+        if (g_mma_trace && (idx) < 64)                                                               \
+            g_mma_trace[((size_t)(blockIdx.y * gridDim.x + blockIdx.x) * 8 + (slot)) * 64 + (idx)] = \
+                (unsigned long long)clock64();                                                       \
+    } while (0)
 #else
+#define MTC(slot, idx) \
+    do {               \
+    } while (0)
 #define MTR(slot, idx) \
     do {               \
     } while (0)
@@ -75,21 +85,30 @@ constexpr int kUnitK = 256;    // weights per row in one raw stage
 constexpr int kSubK = 64;      // weights per row in one A stage (four MMA K-steps of 16)
 constexpr int kWarpRaw = 0, kWarpMma = 1, kWarpX = 2, kWarpDec0 = 3, kDecWarps = 16;
 constexpr int kThreads = (kWarpDec0 + kDecWarps) * 32;
-constexpr int kMaxBPad = 128;
 constexpr int kMaxCluster = 8;
-constexpr int kMaxStages = 8;          // per ring (raw, X, A)
+constexpr int kMaxStages = 8;          // per ring (raw, X, D)
+constexpr int kAStages = 4;            // A stages in tensor memory (32 columns each)
+constexpr int kLag = 2;                // sub-chunks between a decode and its group epilogue
 constexpr int kMinSmem = 120 * 1024;   // keeps a second CTA (and its tensor memory) off the SM
-constexpr uint32_t kTmemCols = 512;    // D in columns [0, 2 b_pad), A stages of 64 columns above it
+constexpr uint32_t kTmemCols = 512;    // A stages in [0, 128), accumulator sets above
+constexpr uint32_t kDCol0 = 32 * kAStages;
 constexpr uint32_t kSmemBudget = 227u * 1024u;
+constexpr uint32_t kFinalOff = 64u * 1024u;  // per-tile result [b][128] after the group combine
+
+// Largest padded batch per launch: the accumulators of kLag + 1 sub-chunks must
+// fit in tensor memory (Q6_K has four 16-weight groups per sub-chunk).
+__host__ __device__ constexpr int max_bpad(int type) { return type == QDQ_Q6_K ? 32 : 64; }
+__host__ __device__ constexpr int groups_per_sub(int type) { return type == QDQ_Q6_K ? 4 : 2; }
 
 struct MmaArgs {
     const uint8_t *W;   // rows x row_bytes
     const uint8_t *xs;  // split X: per K-step of 16 columns, 2 b_pad rows x 16 bf16 (64 b_pad bytes)
+    const float *xsum;  // Q4_K: sum of x over each 32-column group, [cols / 32][b_pad]
     float *y;           // [batch][rows]
     int64_t rows, cols, row_bytes;
     int64_t rows_full;  // rows reached through the tensor map (a multiple of g)
     int batch, b_pad, nunits;
-    int nraw, nx, na;   // ring depths: raw W stages, X stages, A stages (tensor memory)
+    int nraw, nx, nd;   // ring depths: raw W stages, X stages, accumulator sets
     // Raw stage geometry. Rows are grouped in super-rows of g rows, the fewest
     // whose byte length is a multiple of 16, so that W can be described as a 2-D
     // tensor [rows / g][g row_bytes] for the tensor-copy engine. A stage holds
@@ -98,7 +117,7 @@ struct MmaArgs {
     // Rows past rows_full (fewer than g, all in the last tile) are copied row by
     // row into a leftover area at left_off.
     int g, box_inner, kbh, nh;  // kbh: blocks per box
-    uint32_t region_bytes, half_bytes, left_off, left_pitch, stage_bytes, acol0;
+    uint32_t region_bytes, half_bytes, left_off, left_pitch, stage_bytes, pad2;
 };
 
 struct Layout {
@@ -109,8 +128,8 @@ __host__ __device__ inline Layout layout_for(uint32_t stage_bytes, int nraw, int
     Layout L;
     L.x = (uint32_t)nraw * stage_bytes;
     L.x_stage = (uint32_t)(256 * b_pad);  // four K-steps of 2 b_pad rows x 16 bf16
-    L.bars = (L.x + (uint32_t)nx * L.x_stage + 127u) & ~127u;
-    L.tmem_slot = L.bars + 8u * (6 * kMaxStages + 1);
+    L.bars = (L.x + (uint32_t)nx * L.x_stage + 127u) & ~127u;  // nx = kAStages
+    L.tmem_slot = L.bars + 8u * (6 * kMaxStages + 2 * kAStages);
     L.total = L.tmem_slot + 16u;
     if (L.total < (uint32_t)kMinSmem) L.total = kMinSmem;
     return L;
@@ -145,21 +164,6 @@ QDQ_DEV void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Two 32-lane x 16-column loads and their completion wait in one statement, so
-// no use of the registers can be scheduled before the wait.
-QDQ_DEV void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
-        "[%33];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
-          "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
-          "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
-          "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
-        : "r"(ta), "r"(tb)
-        : "memory");
-}
 QDQ_DEV void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
                  "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
@@ -186,11 +190,6 @@ QDQ_DEV uint32_t lds_u16(uint32_t a) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
     return v;
 }
-QDQ_DEV uint64_t fmul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 
 // Instruction descriptor of kind::f16: fp32 D (bits 4-5 = 1), bf16 A and B (bits
 // 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22,
@@ -208,7 +207,7 @@ QDQ_DEV uint64_t make_sdesc(uint32_t saddr) {
            (1ull << 46);
 }
 
-// w -> (bf16(w), bf16(w - bf16(w))) for two weights; the first weight of the pair
+// x -> (bf16(x), bf16(x - bf16(x))) for two values; the first value of the pair
 // (lower address) goes to the low half of each packed word.
 QDQ_DEV void split_pair(uint64_t w2, uint32_t &hi, uint32_t &lo) {
     uint32_t h, l;
@@ -219,102 +218,149 @@ QDQ_DEV void split_pair(uint64_t w2, uint32_t &hi, uint32_t &lo) {
     lo = l;
 }
 
+// ---- exact bf16 quants ------------------------------------------------------------
+// 0x43 in the high byte of a 16-bit lane is the bf16 exponent of 128 with a unit
+// last mantissa place, so a byte v < 128 placed in the low byte reads as the bf16
+// 128 + v, exactly; one bf16 subtraction of (128 + offset) then leaves v - offset,
+// exactly (a small integer). Selector 0x4140 takes bytes 0 and 1 of w, 0x4342 bytes
+// 2 and 3.
+QDQ_DEV uint32_t bf16_biased_pair(uint32_t w, uint32_t sel) { return __byte_perm(w, 0x43434343u, sel); }
+QDQ_DEV uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+constexpr uint32_t kBf16x2_128 = 0x43004300u;  // (128, 128)
+constexpr uint32_t kBf16x2_136 = 0x43084308u;  // (136, 136): q4_0 offset 8
+constexpr uint32_t kBf16x2_160 = 0x43204320u;  // (160, 160): Q6_K offset 32
+
 QDQ_DEV uint64_t magic_pair(uint32_t w, int first) {
     return first == 0 ? bits2(byte_to_magic<0>(w), byte_to_magic<1>(w)) : bits2(byte_to_magic<2>(w), byte_to_magic<3>(w));
 }
 
-// ---- decoders: one run of 16 consecutive weights of one row ----------------------
-// A sub-chunk (64 weights of a row) has four runs; run r = 2 h + p. Each decoder
-// fills w2[8] (the run's weights as fp32 pairs) and returns the run's first
-// octet (8 weights) within the sub-chunk.
+// One run: 16 consecutive quants of one row in a sub-chunk (run r = 2 h + p of four).
+// The decoder writes them as eight packed bf16 pairs and returns the run's first
+// octet (8 quants) in the sub-chunk and the scale(s) of the run's group.
+struct Run {
+    uint32_t q[8];
+    int octet;
+    float s, m;  // w = s q - m
+};
 
 // Q4_K: chunk `sub` holds sub-blocks 2 sub (low nibbles) and 2 sub + 1 (high
-// nibbles); half h takes bytes 16h..16h+15 of the chunk, p picks the nibble.
-// w = q (d sc) - dmin mn.
-QDQ_DEV int decode_q4k(uint32_t blk, int sub, int h, int p, uint64_t (&w2)[8]) {
+// nibbles); half h takes bytes 16h..16h+15 of the chunk, p picks the nibble, so
+// the group is sub-block 2 sub + p with s = d sc, m = dmin mn.
+QDQ_DEV void run_q4k(uint32_t blk, int sub, int h, int p, Run &o) {
     const uint4 H = lds128(blk);
     const uint4 V = lds128(blk + 16 + 32 * sub + 16 * h);
     uint32_t sc2, mn2;
     q4k_pair_fields(H.y, H.z, H.w, sub, &sc2, &mn2);
-    const float d = half_bits_to_float(H.x & 0xFFFF), dmin = half_bits_to_float(H.x >> 16);
-    const float dsc = __fmul_rn(d, (float)((sc2 >> (8 * p)) & 0xFF));
-    const float dmn = __fmul_rn(dmin, (float)((mn2 >> (8 * p)) & 0xFF));
-    const uint64_t s2 = pack2(dsc, dsc), m2 = pack2(-dmn, -dmn), two23 = pack2(kTwo23, kTwo23);
+    o.s = __fmul_rn(half_bits_to_float(H.x & 0xFFFF), (float)((sc2 >> (8 * p)) & 0xFF));
+    o.m = __fmul_rn(half_bits_to_float(H.x >> 16), (float)((mn2 >> (8 * p)) & 0xFF));
     const uint32_t v[4] = {V.x, V.y, V.z, V.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t nib = (v[i] >> (4 * p)) & 0x0F0F0F0Fu;
-        w2[2 * i] = ffma2(fsub2(magic_pair(nib, 0), two23), s2, m2);
-        w2[2 * i + 1] = ffma2(fsub2(magic_pair(nib, 2), two23), s2, m2);
+        o.q[2 * i] = bf16x2_sub(bf16_biased_pair(nib, 0x4140), kBf16x2_128);
+        o.q[2 * i + 1] = bf16x2_sub(bf16_biased_pair(nib, 0x4342), kBf16x2_128);
     }
-    return p == 0 ? 2 * h : 4 + 2 * h;
+    o.octet = p == 0 ? 2 * h : 4 + 2 * h;
 }
 
 // Q6_K: sub-chunk `sub` is half hp = sub / 2 of the block, run k = 2 (sub & 1) + h;
 // element 128 hp + 32 k + l (l = 16 p .. 16 p + 15 here) has scale index
-// 8 hp + 2 k + p. w = (d sc) (q6 - 32).
-QDQ_DEV int decode_q6k(uint32_t blk, int sub, int h, int p, uint64_t (&w2)[8]) {
+// 8 hp + 2 k + p: the run is exactly one scale group. s = d sc, q = q6 - 32.
+QDQ_DEV void run_q6k(uint32_t blk, int sub, int h, int p, Run &o) {
     const int hp = sub >> 1, k = 2 * (sub & 1) + h;
     uint32_t ql[4], qh[4];
     lds_words_a2<4>(blk + 64 * hp + 32 * h + 16 * p, ql);  // run k & 1 == h
     lds_words_a2<4>(blk + 128 + 32 * hp + 16 * p, qh);
     const uint32_t scw = lds_u16(blk + 192 + 8 * hp + 2 * k);
-    const float d = half_bits_to_float(lds_u16(blk + 208));
-    const float dsc = __fmul_rn(d, (float)(int8_t)((scw >> (8 * p)) & 0xFF));
-    const uint64_t s2 = pack2(dsc, dsc);
-    const float off = kTwo23 + 32.0f;
-    const uint64_t off2 = pack2(off, off);
+    o.s = __fmul_rn(half_bits_to_float(lds_u16(blk + 208)), (float)(int8_t)((scw >> (8 * p)) & 0xFF));
+    o.m = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t q6 = q6k_quant_bytes(ql[i], qh[i], k);
-        w2[2 * i] = fmul2(fsub2(magic_pair(q6, 0), off2), s2);
-        w2[2 * i + 1] = fmul2(fsub2(magic_pair(q6, 2), off2), s2);
+        o.q[2 * i] = bf16x2_sub(bf16_biased_pair(q6, 0x4140), kBf16x2_160);
+        o.q[2 * i + 1] = bf16x2_sub(bf16_biased_pair(q6, 0x4342), kBf16x2_160);
     }
-    return 4 * h + 2 * p;
+    o.octet = 4 * h + 2 * p;
 }
 
-// q8_0 (PETIT): the block at b (block 2 sub + h of the unit): fp32 d then 32
-// int8; run p is int8 16p..16p+15. w = d q.
-QDQ_DEV int decode_q8_0(uint32_t b, int h, int p, uint64_t (&w2)[8]) {
-    const float d = __uint_as_float(lds32(b));
-    const uint64_t d2 = pack2(d, d);
+// q8_0 (PETIT): the block at b (block 2 sub + h of the unit, the run's group):
+// fp32 d then 32 int8; run p is int8 16p..16p+15. s = d. int8 -> fp32 exactly by
+// exponent-field construction, then to bf16 (exact: |q| < 2^8).
+QDQ_DEV void run_q8_0(uint32_t b, int h, int p, Run &o) {
+    o.s = __uint_as_float(lds32(b));
+    o.m = 0.0f;
     const float off = kTwo23 + 128.0f;
     const uint64_t off2 = pack2(off, off);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t v = lds32(b + 4 + 16 * p + 4 * i) ^ 0x80808080u;  // int8 -> q + 128
-        w2[2 * i] = fmul2(fsub2(magic_pair(v, 0), off2), d2);
-        w2[2 * i + 1] = fmul2(fsub2(magic_pair(v, 2), off2), d2);
+        const uint64_t f01 = fsub2(magic_pair(v, 0), off2), f23 = fsub2(magic_pair(v, 2), off2);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.q[2 * i]) : "f"(hi_of(f01)), "f"(lo_of(f01)));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.q[2 * i + 1]) : "f"(hi_of(f23)), "f"(lo_of(f23)));
     }
-    return 4 * h + 2 * p;
+    o.octet = 4 * h + 2 * p;
 }
 
-// q4_0 (PETIT): the block at b (block 2 sub + h of the unit): fp16 d then 16
-// bytes whose low nibbles are weights 0-15 and high nibbles weights 16-31; run p
-// takes the low (p = 0) or high nibbles. w = (q - 8) d.
-QDQ_DEV int decode_q4_0(uint32_t b, int h, int p, uint64_t (&w2)[8]) {
-    const float d = half_bits_to_float(lds_u16(b));
+// q4_0 (PETIT): the block at b (block 2 sub + h of the unit, the run's group):
+// fp16 d then 16 bytes whose low nibbles are weights 0-15 and high nibbles weights
+// 16-31; run p takes the low (p = 0) or high nibbles. s = d, q = nibble - 8.
+QDQ_DEV void run_q4_0(uint32_t b, int h, int p, Run &o) {
+    o.s = half_bits_to_float(lds_u16(b));
+    o.m = 0.0f;
     uint32_t qs[4];
     lds_words_a2<4>(b + 2, qs);
-    const uint64_t d2 = pack2(d, d);
-    const float off = kTwo23 + 8.0f;
-    const uint64_t off2 = pack2(off, off);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t nib = (qs[i] >> (4 * p)) & 0x0F0F0F0Fu;
-        w2[2 * i] = fmul2(fsub2(magic_pair(nib, 0), off2), d2);
-        w2[2 * i + 1] = fmul2(fsub2(magic_pair(nib, 2), off2), d2);
+        o.q[2 * i] = bf16x2_sub(bf16_biased_pair(nib, 0x4140), kBf16x2_136);
+        o.q[2 * i + 1] = bf16x2_sub(bf16_biased_pair(nib, 0x4342), kBf16x2_136);
     }
-    return 4 * h + 2 * p;
+    o.octet = 4 * h + 2 * p;
 }
 
 template <int TYPE>
-QDQ_DEV int decode_run(uint32_t blk, int sub, int h, int p, uint64_t (&w2)[8]) {
-    if constexpr (TYPE == QDQ_Q4_K) return decode_q4k(blk, sub, h, p, w2);
-    else if constexpr (TYPE == QDQ_Q6_K) return decode_q6k(blk, sub, h, p, w2);
-    else if constexpr (TYPE == QDQ_Q8_0) return decode_q8_0(blk, h, p, w2);
-    else return decode_q4_0(blk, h, p, w2);
+QDQ_DEV void decode_run(uint32_t blk, int sub, int h, int p, Run &o) {
+    if constexpr (TYPE == QDQ_Q4_K) run_q4k(blk, sub, h, p, o);
+    else if constexpr (TYPE == QDQ_Q6_K) run_q6k(blk, sub, h, p, o);
+    else if constexpr (TYPE == QDQ_Q8_0) run_q8_0(blk, h, p, o);
+    else run_q4_0(blk, h, p, o);
 }
+
+// tcgen05.ld of 8 columns of this warp's lanes, with its completion wait.
+QDQ_DEV void tmem_ld8(uint32_t ta, uint32_t (&v)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+        : "r"(ta)
+        : "memory");
+}
+
+// A shared-memory descriptor from its low word (start address, leading offset)
+// and high word. Building each MMA's descriptor as a 32-bit add on a
+// loop-invariant base keeps the MMA issue at about 10 ns; composing the 64-bit
+// value per MMA costs several times that.
+QDQ_DEV uint64_t desc_from_words(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
+// A ring slot and its phase, advanced one use at a time (no divisions).
+struct Ring {
+    int slot = 0, phase = 0, n;
+    QDQ_DEV explicit Ring(int n_) : n(n_) {}
+    QDQ_DEV void next() {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1;
+        }
+    }
+};
 
 QDQ_DEV int unit_k(const MmaArgs &a, int u) {
     const int64_t left = a.cols - (int64_t)u * kUnitK;
@@ -337,6 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kBB = TYPE == QDQ_Q4_K ? 144 : TYPE == QDQ_Q6_K ? 210 : TYPE == QDQ_Q8_0 ? 36 : 18;
     constexpr int kBW = (TYPE == QDQ_Q4_K || TYPE == QDQ_Q6_K) ? 256 : 32;
     constexpr int kUnitBytes = (kUnitK / kBW) * kBB;  // bytes of a full unit of one row
+    constexpr int kG = groups_per_sub(TYPE);         // scale groups per sub-chunk
+    constexpr int kKbh = TYPE == QDQ_Q8_0 ? 4 : kUnitK / kBW;  // blocks per box row
     extern __shared__ __align__(1024) uint8_t smem[];
     const Layout L = layout_for(a.stage_bytes, a.nraw, a.nx, a.b_pad);
     const uint32_t sb = smem_u32(smem);
@@ -350,27 +398,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int trows = (int)(a.rows_full - row0 <= 0 ? 0 : (a.rows_full - row0 < kM ? a.rows_full - row0 : kM));
     const int nleft = rows_here - trows;
     const int u0 = (int)((int64_t)a.nunits * rank / S), u1 = (int)((int64_t)a.nunits * (rank + 1) / S);
-    const int b_pad = a.b_pad, nraw = a.nraw, nx = a.nx, na = a.na;
+    const int b_pad = a.b_pad, nraw = a.nraw, nd = a.nd;
+    const uint32_t dset = (uint32_t)(kG * b_pad);  // accumulator columns of one sub-chunk
 
     const uint32_t raw_full = sb + L.bars, raw_empty = raw_full + 8 * kMaxStages;
-    const uint32_t x_full = raw_empty + 8 * kMaxStages, x_empty = x_full + 8 * kMaxStages;
-    const uint32_t a_full = x_empty + 8 * kMaxStages, a_empty = a_full + 8 * kMaxStages;
-    const uint32_t acc_full = a_empty + 8 * kMaxStages;
+    const uint32_t d_full = raw_empty + 8 * kMaxStages, d_empty = d_full + 8 * kMaxStages;
+    const uint32_t a_full = d_empty + 8 * kMaxStages, a_empty = a_full + 8 * kAStages;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nraw; ++s) {
             mbar_init(raw_full + 8 * s, 1);
             mbar_init(raw_empty + 8 * s, kDecWarps);
         }
-        for (int s = 0; s < nx; ++s) {
-            mbar_init(x_full + 8 * s, 1);
-            mbar_init(x_empty + 8 * s, 1);
+        for (int s = 0; s < nd; ++s) {
+            mbar_init(d_full + 8 * s, 1);
+            mbar_init(d_empty + 8 * s, kDecWarps);
         }
-        for (int s = 0; s < na; ++s) {
-            mbar_init(a_full + 8 * s, kDecWarps);
+        // an A stage is full when the 16 decode warps have stored its quants and the
+        // sub-chunk's split X has landed (the X producer's arrival carries the bytes)
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(a_full + 8 * s, kDecWarps + 1);
             mbar_init(a_empty + 8 * s, 1);
         }
-        mbar_init(acc_full, 1);
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -382,21 +431,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // the same value in every lane, and known to the compiler as warp-uniform
     const uint32_t tmem = __shfl_sync(0xFFFFFFFFu, *reinterpret_cast<volatile uint32_t *>(smem + L.tmem_slot), 0);
-    if (threadIdx.x == 0) MTR(7, 0);
+    if (threadIdx.x == 0) MTC(7, 0);
 
     if (warp == kWarpRaw) {
         // ---- raw weight blocks: tensor boxes, plus leftover rows one by one --------
         const uint64_t pol = policy_evict_first();
         const uintptr_t wend16 = (uintptr_t)(a.W + a.rows * a.row_bytes) & ~(uintptr_t)15;
+        Ring rs(nraw);
         bool ok = true;
-        for (int u = u0, i = 0; u < u1; ++u, ++i) {
-            const int s = i % nraw;
-            if (i >= nraw) ok = mbar_wait(raw_empty + 8 * s, ((i / nraw) + 1) & 1, status);
+        for (int u = u0, i = 0; u < u1; ++u, ++i, rs.next()) {
+            const int s = rs.slot;
+            if (i >= nraw) ok = mbar_wait(raw_empty + 8 * s, rs.phase ^ 1, status);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             const int uk = unit_k(a, u);
             const int ub = (uk / kBW) * kBB;
             const uint32_t stage = sb + (uint32_t)s * a.stage_bytes;
-            const int nh_u = (uk / kBW) > a.kbh ? a.nh : 1;  // a short last unit may need one box
+            const int nh_u = (uk / kBW) > kKbh ? a.nh : 1;  // a short last unit may need one box
             // leftover row lane (< g - 1 of them): 1-D copy from its 16-byte boundary
             uintptr_t src_al = 0;
             uint32_t dst = 0, nbytes = 0;
@@ -425,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int y = (int)(row0 / a.g);
                     for (int hb = 0; hb < nh_u; ++hb)
                         for (int m = 0; m < a.g; ++m) {
-                            const int64_t off = (int64_t)m * a.row_bytes + (int64_t)u * kUnitBytes + hb * a.kbh * kBB;
+                            const int64_t off = (int64_t)m * a.row_bytes + (int64_t)u * kUnitBytes + hb * kKbh * kBB;
                             tma_load_2d(stage + hb * a.half_bytes + m * a.region_bytes, &wmap, (int)(off & ~(int64_t)15),
                                         y, raw_full + 8 * s, pol);
                         }
@@ -433,24 +483,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (nbytes) bulk_g2s_hint(dst, (const void *)src_al, nbytes, raw_full + 8 * s, pol);
-            if (lane == 0) MTR(0, i);
         }
     } else if (warp == kWarpX) {
-        // ---- split X, one bulk copy per sub-chunk ----------------------------------
+        // ---- split X, one bulk copy per sub-chunk, into the X slot of the A stage ---
         if (lane == 0) {
-            int j = 0;
+            Ring rx(kAStages);
             bool ok = true;
+            int j = 0;
             for (int u = u0; u < u1 && ok; ++u) {
                 const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-                for (int sub = 0; sub < ns; ++sub, ++j) {
-                    const int s = j % nx;
-                    if (j >= nx && !(ok = mbar_wait(x_empty + 8 * s, ((j / nx) + 1) & 1, status))) break;
+                for (int sub = 0; sub < ns; ++sub, ++j, rx.next()) {
+                    const int s = rx.slot;
+                    if (j >= kAStages && !(ok = mbar_wait(a_empty + 8 * s, rx.phase ^ 1, status))) break;
                     const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
                     const int64_t kstep0 = ((int64_t)u * kUnitK + kSubK * sub) / 16;
                     const uint32_t bytes = (uint32_t)(ks * 64 * b_pad);
-                    mbar_arrive_expect_tx(x_full + 8 * s, bytes);
-                    bulk_g2s(sb + L.x + s * L.x_stage, a.xs + kstep0 * 64 * b_pad, bytes, x_full + 8 * s);
-                    MTR(4, j);
+                    mbar_arrive_expect_tx(a_full + 8 * s, bytes);
+                    bulk_g2s(sb + L.x + s * L.x_stage, a.xs + kstep0 * 64 * b_pad, bytes, a_full + 8 * s);
                 }
             }
         }
@@ -458,122 +507,218 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
         // ---- MMA issue: the whole warp runs the loop with warp-uniform operands and
         // one elected lane issues, so the descriptors stay in uniform registers (a
-        // lone thread issuing from per-thread registers reaches a tenth of the rate)
-        const uint32_t tm = tmem;
-        const uint32_t idesc2 = make_idesc(2 * b_pad), idesc1 = make_idesc(b_pad);
-        int j = 0;
+        // lone thread issuing from per-thread registers reaches a tenth of the rate).
+        // Per K-step t of a sub-chunk: Z_g += q x_hi and Z_g += q x_lo into the
+        // accumulator region of t's group.
+        const uint32_t idesc = make_idesc(b_pad);
+        const uint64_t xdesc = make_sdesc(sb + L.x);  // X slot 0, K-step 0
+        const uint32_t xdesc_lo = (uint32_t)xdesc, xdesc_hi = (uint32_t)(xdesc >> 32);
+        const uint32_t slot_step = L.x_stage >> 4, kstep_step = (64u * b_pad) >> 4;
+        const uint32_t lo_step = (32u * b_pad) >> 4;  // the x_lo rows follow the x_hi rows
+        Ring ra(kAStages), rd(nd);
         bool ok = true;
+        int j = 0;
         for (int u = u0; u < u1 && ok; ++u) {
             const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-            for (int sub = 0; sub < ns; ++sub, ++j) {
-                const int sa = j % na, sx = j % nx;
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_full + 8 * sa, (j / na) & 1, status));
-                if (lane == 0) MTR(5, j);
-                ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait(x_full + 8 * sx, (j / nx) & 1, status));
-                if (lane == 0) MTR(6, j);
+            for (int sub = 0; sub < ns; ++sub, ++j, ra.next(), rd.next()) {
+                if (lane == 0 && j < 8) MTC(7, 16 + j);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_full + 8 * ra.slot, ra.phase, status));
+                if (lane == 0) MTC(5, j);
+                if (ok && j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_empty + 8 * rd.slot, rd.phase ^ 1, status));
+                if (lane == 0) MTC(6, j);
                 if (!ok) break;
                 tc_fence_after();
+                if (lane == 0 && j < 8) MTC(7, 40 + j);
                 const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
-                const uint32_t xbase = sb + L.x + sx * L.x_stage, abase = tm + a.acol0 + 64 * sa;
-                for (int t = 0; t < ks; ++t) {
-                    const uint64_t bdesc = make_sdesc(xbase + t * 64 * b_pad);
-                    const uint32_t acc = (j | t) != 0;
-                    if (elect_one()) {
-                        mma_ts(tm, abase + 8 * t, bdesc, idesc2, acc);  // hi x [x_hi; x_lo]
-                        mma_ts(tm, abase + 32 + 8 * t, bdesc, idesc1, 1u);  // lo x x_hi
+                const uint32_t blo = xdesc_lo + ra.slot * slot_step;
+                const uint32_t abase = tmem + 32u * ra.slot, dbase = tmem + kDCol0 + rd.slot * dset;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    if (t < ks) {
+                        const uint32_t bt = blo + t * kstep_step;
+                        const uint32_t dg = dbase + ((kG == 4) ? t : (t >> 1)) * b_pad;
+                        const uint32_t acc = (kG == 4) ? 0u : (uint32_t)(t & 1);  // first write of the region
+                        if (elect_one()) {
+                            mma_ts(dg, abase + 8 * t, desc_from_words(bt, xdesc_hi), idesc, acc);
+                            mma_ts(dg, abase + 8 * t, desc_from_words(bt + lo_step, xdesc_hi), idesc, 1u);
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
+                if (lane == 0 && j < 8) MTC(7, 32 + j);
                 if (elect_one()) {
-                    mma_commit(a_empty + 8 * sa);
-                    mma_commit(x_empty + 8 * sx);
+                    mma_commit(a_empty + 8 * ra.slot);
+                    mma_commit(d_full + 8 * rd.slot);
                 }
                 __syncwarp();
+                if (lane == 0 && j < 8) MTC(7, 24 + j);
             }
         }
-        if (ok && elect_one()) mma_commit(acc_full);
-        __syncwarp();
     } else {
-        // ---- decode ------------------------------------------------------------------
+        // ---- decode, and the group epilogue two sub-chunks behind --------------------
         const int dw = warp - kWarpDec0, run = dw >> 2, h = run >> 1, p = run & 1;
         const int q = warp & 3, rr = 32 * q + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
         // this row's place in a stage: region m, row s (tensor rows), or the leftover
         // area; rows past the matrix read row 0 of region 0 (their results are dropped)
-        const int rm = rr < trows ? rr % a.g : 0, rs = rr < trows ? rr / a.g : 0;
+        const int rm = rr < trows ? rr % a.g : 0, rsr = rr < trows ? rr / a.g : 0;
         const uint32_t row_off =
-            rr < trows ? (uint32_t)rm * a.region_bytes + (uint32_t)rs * a.box_inner
+            rr < trows ? (uint32_t)rm * a.region_bytes + (uint32_t)rsr * a.box_inner
                        : (rr < rows_here ? a.left_off + (uint32_t)(rr - trows) * a.left_pitch : 0u);
         const int64_t row_phase = rr < trows ? (int64_t)rm * a.row_bytes : (row0 + rr) * a.row_bytes;
+        // the accumulator this thread reads back: its run's group, and its share of
+        // the batch columns (all of them for Q6_K, whose runs are whole groups)
+        const int grp = (kG == 4) ? run : (TYPE == QDQ_Q4_K ? p : h);
+        const int cw = (kG == 4) ? b_pad : b_pad / 2;
+        const int col0 = (kG == 4) ? 0 : (TYPE == QDQ_Q4_K ? h : p) * (b_pad / 2);
+        float yacc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) yacc[i] = 0.0f;
+        // scales of the last kLag decoded sub-chunks (slot = sub-chunk index & 1)
+        // scales of the last two decoded sub-chunks (even / odd sub-chunk index)
+        float s_ev = 0.f, m_ev = 0.f, s_od = 0.f, m_od = 0.f;
+        int g_ev = -1, g_od = -1;  // global 32-column group of the scale; < 0: group absent
+        int rd_s = 0, rd_p = 0, rd_count = 0;
+        auto rd_slot = [&]() { return rd_s; };
+        auto rd_phase = [&]() { return rd_p; };
+        auto rd_next = [&]() {
+            if (++rd_s == nd) {
+                rd_s = 0;
+                rd_p ^= 1;
+            }
+        };
+
+        // epilogue of one sub-chunk: read back this thread's accumulator columns and
+        // add s Z (- m X_g) into yacc; then release the accumulator set
+        auto epilogue = [&](float sc, float mn, int gg) -> bool {
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * rd_slot(), rd_phase(), status))) return false;
+            if (lane == 0 && dw < 8 && rd_count < 8) MTC(3, dw * 8 + rd_count);
+            tc_fence_after();
+            const uint32_t dcol = tl + kDCol0 + (uint32_t)rd_slot() * dset + grp * b_pad + col0;
+#pragma unroll
+            for (int c8 = 0; c8 < 4; ++c8) {
+                if (8 * c8 < cw) {
+                    uint32_t v[8];
+                    tmem_ld8(dcol + 8 * c8, v);
+                    if (gg >= 0) {
+                        if constexpr (TYPE == QDQ_Q4_K) {
+                            const float4 *xg =
+                                reinterpret_cast<const float4 *>(a.xsum + (int64_t)gg * b_pad + col0 + 8 * c8);
+                            const float4 x0 = __ldg(xg), x1 = __ldg(xg + 1);
+                            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int t = 0; t < 8; ++t)
+                                yacc[8 * c8 + t] = fmaf(sc, __uint_as_float(v[t]), fmaf(-mn, xv[t], yacc[8 * c8 + t]));
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 8; ++t)
+                                yacc[8 * c8 + t] = fmaf(sc, __uint_as_float(v[t]), yacc[8 * c8 + t]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(d_empty + 8 * rd_slot());
+            if (lane == 0 && dw < 8 && rd_count < 8) MTC(4, dw * 8 + rd_count);
+            ++rd_count;
+            rd_next();
+            return true;
+        };
+
+        // sub-chunks of this CTA: four per full unit, fewer for a short last unit
+        const int J = (u1 - u0) * (kUnitK / kSubK) -
+                      (u1 == a.nunits ? (kUnitK / kSubK) - (unit_k(a, u1 - 1) + kSubK - 1) / kSubK : 0);
+        Ring rs(nraw), ra(kAStages);
         bool ok = true;
-        int j = 0;
-        for (int u = u0, i = 0; u < u1 && ok; ++u, ++i) {
-            const int s = i % nraw;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(raw_full + 8 * s, (i / nraw) & 1, status));
-            if (!ok) break;
-            const uint32_t stage = sb + (uint32_t)s * a.stage_bytes + row_off;
-            const int64_t unit_phase = row_phase + (int64_t)u * kUnitBytes;
-            const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-            for (int sub = 0; sub < ns; ++sub, ++j) {
-                const int sa = j % na;
-                if (j >= na) {
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_empty + 8 * sa, ((j / na) + 1) & 1, status));
+        int u = u0, sub = 0, ns = 0, uk = 0;
+        uint32_t blk0 = 0, blk1 = 0;  // this row's data in the stage: first / second box half
+        for (int j = 0; j < J + kLag && ok; ++j) {
+            float s_new = 0.f, m_new = 0.f;
+            int g_new = -1;
+            if (lane == 0 && dw < 8 && j < 8) MTC(0, dw * 8 + j);
+            if (j < J) {
+                if (sub == 0) {  // a new unit: wait for its raw stage, place this row in it
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(raw_full + 8 * rs.slot, rs.phase, status));
+                    if (!ok) break;
+                    uk = unit_k(a, u);
+                    ns = (uk + kSubK - 1) / kSubK;
+                    const uint32_t stage = sb + (uint32_t)rs.slot * a.stage_bytes + row_off;
+                    const int64_t unit_phase = row_phase + (int64_t)u * kUnitBytes;
+                    if (rr < trows) {
+                        blk0 = stage + (uint32_t)(unit_phase & 15);
+                        blk1 = stage + a.half_bytes + (uint32_t)((unit_phase + kKbh * kBB) & 15);
+                    } else {
+                        blk0 = stage + (uint32_t)(unit_phase & 15);
+                        blk1 = blk0 + kKbh * kBB;
+                    }
+                }
+                if (j >= kAStages) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_empty + 8 * ra.slot, ra.phase ^ 1, status));
                     if (!ok) break;
                     tc_fence_after();
                 }
-                if (lane == 0 && dw < 8 && j < 8) MTR(2, dw * 8 + j);
+                if (lane == 0 && dw < 8 && j < 8) MTC(1, dw * 8 + j);
                 // the block this thread decodes: the unit's block (K-quants), or
                 // block 2 sub + h of the unit (q8_0 / q4_0)
-                const int kb = (kBW == 256) ? 0 : 2 * sub + h;
-                uint32_t blk;
-                if (rr < trows) {
-                    const int hb = kb / a.kbh;
-                    const uint32_t lead = (uint32_t)((unit_phase + hb * a.kbh * kBB) & 15);
-                    blk = stage + hb * a.half_bytes + lead + (uint32_t)(kb % a.kbh) * kBB;
-                } else {
-                    blk = stage + (uint32_t)(unit_phase & 15) + (uint32_t)kb * kBB;
+                uint32_t blk = blk0;
+                if constexpr (kBW == 32) {
+                    const int kb = 2 * sub + h;
+                    blk = (kb < kKbh ? blk0 : blk1) + (uint32_t)(kb & (kKbh - 1)) * kBB;
                 }
-                uint64_t w2[8];
-                const int o = decode_run<TYPE>(blk, sub, h, p, w2);
-                uint32_t hi[8], lo[8];
-#pragma unroll
-                for (int i2 = 0; i2 < 8; ++i2) split_pair(w2[i2], hi[i2], lo[i2]);
-                const uint32_t col = tl + a.acol0 + 64 * sa + 4 * o;
-                tmem_st8(col, hi);
-                tmem_st8(col + 32, lo);
-                if (lane == 0 && dw < 8 && j < 8) MTR(1, dw * 8 + j);
+                Run rn;
+                decode_run<TYPE>(blk, sub, h, p, rn);
+                tmem_st8(tl + 32u * ra.slot + 4 * rn.octet, rn.q);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0 && dw < 8 && j < 8) MTR(3, dw * 8 + j);
-                if (lane == 0) mbar_arrive(a_full + 8 * sa);
+                if (lane == 0) mbar_arrive(a_full + 8 * ra.slot);
+                if (lane == 0 && dw < 8 && j < 8) MTC(2, dw * 8 + j);
+                ra.next();
+                s_new = rn.s;
+                m_new = rn.m;
+                // the group is present unless a short last sub-chunk (q8_0 / q4_0) ends first
+                if (grp * (kSubK / kG) < uk - kSubK * sub) g_new = 8 * u + 2 * sub + grp;
+                // advance (u, sub); release the raw stage after its last sub-chunk
+                if (++sub == ns) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(raw_empty + 8 * rs.slot);
+                    rs.next();
+                    sub = 0;
+                    ++u;
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(raw_empty + 8 * s);
+            const bool odd = j & 1;  // sub-chunk j - 2 has the same parity
+            if (j >= kLag) ok = odd ? epilogue(s_od, m_od, g_od) : epilogue(s_ev, m_ev, g_ev);
+            if (odd) {
+                s_od = s_new;
+                m_od = m_new;
+                g_od = g_new;
+            } else {
+                s_ev = s_new;
+                m_ev = m_new;
+                g_ev = g_new;
+            }
         }
 
-        // ---- epilogue: D (lane = row, column = batch) -> y or the cluster partials --
-        if (run == 0) {
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full, 0, status));
-            if (q == 0 && lane == 0) MTR(7, 1);
-            if (ok) {
-                tc_fence_after();
-                float *red = reinterpret_cast<float *>(smem);
-                for (int n0 = 0; n0 < a.batch; n0 += 16) {
-                    uint32_t v0[16], v1[16];
-                    tmem_ld16x2(tl + n0, tl + b_pad + n0, v0, v1);
+        // ---- combine the groups of each row: slot buffer [grp][n][128] at offset 0 --
+        float *slotbuf = reinterpret_cast<float *>(smem);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int n = n0 + t;
-                        const float val = __uint_as_float(v0[t]) + __uint_as_float(v1[t]);
-                        if (n < a.batch) {
-                            if (S == 1) {
-                                if (rr < rows_here) a.y[(int64_t)n * a.rows + row0 + rr] = val;
-                            } else {
-                                red[n * kM + rr] = val;
-                            }
-                        }
-                    }
+        for (int c8 = 0; c8 < 4; ++c8)
+            if (8 * c8 < cw)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) slotbuf[((grp * b_pad) + col0 + 8 * c8 + t) * kM + rr] = yacc[8 * c8 + t];
+        named_bar_sync(1, kDecWarps * 32);
+        if (run == 0) {
+            float *fin = reinterpret_cast<float *>(smem + kFinalOff);
+            for (int n = 0; n < a.batch; ++n) {
+                float v = 0.0f;
+#pragma unroll
+                for (int g = 0; g < kG; ++g) v += slotbuf[(g * b_pad + n) * kM + rr];
+                if (S == 1) {
+                    if (rr < rows_here) a.y[(int64_t)n * a.rows + row0 + rr] = v;
+                } else {
+                    fin[n * kM + rr] = v;
                 }
             }
         }
@@ -593,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int idx = threadIdx.x; idx < a.batch * nr; idx += kThreads) {
             const int n = idx / nr, r = r_lo + idx % nr;
             if (r < rows_here) {
-                const uint32_t off = sb + (uint32_t)(n * kM + r) * 4u;
+                const uint32_t off = sb + kFinalOff + (uint32_t)(n * kM + r) * 4u;
                 float part[kMaxCluster];
 #pragma unroll
                 for (int c = 0; c < kMaxCluster; ++c)
@@ -612,9 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // x[batch][cols] fp32 -> the split B operand: for each K-step t of 16 columns a
 // block of 2 b_pad rows (x_hi rows 0..b_pad-1, x_lo rows b_pad..2 b_pad-1; rows
-// past the batch are zero) in the canonical K-major layout.
+// past the batch are zero) in the canonical K-major layout; and, when xsum is
+// given, the sum of x over each 32-column group, xsum[group][b_pad].
 __global__ void __launch_bounds__(256) xsplit_kernel(const float *__restrict__ x, int batch, int b_pad, int64_t cols,
-                                                     uint8_t *__restrict__ xs) {
+                                                     uint8_t *__restrict__ xs, float *__restrict__ xsum) {
     const int64_t total = (cols / 16) * b_pad * 2;  // (K-step, row, octet)
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -637,6 +783,24 @@ __global__ void __launch_bounds__(256) xsplit_kernel(const float *__restrict__ x
             make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(blk + ((b_pad + n) >> 3) * 256 + kk * 128 + (n & 7) * 16) =
             make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    if (xsum) {
+        const int64_t ng = (cols / 32) * b_pad;
+        for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < ng;
+             idx += (int64_t)gridDim.x * blockDim.x) {
+            const int n = (int)(idx % b_pad);
+            const int64_t g = idx / b_pad;
+            float acc = 0.0f;
+            if (n < batch) {
+                const float4 *src = reinterpret_cast<const float4 *>(x + (int64_t)n * cols + 32 * g);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v = __ldg(src + i);
+                    acc += (v.x + v.y) + (v.z + v.w);
+                }
+            }
+            xsum[idx] = acc;
+        }
     }
 }
 
@@ -709,13 +873,15 @@ int raw_geometry(int type, const void *W, int64_t rows, int64_t cols, MmaArgs &a
     return QDQ_OK;
 }
 
-// Ring depths: X stages (at least three, about 64 KiB), A stages in the tensor
-// memory above D, and raw stages in the shared memory that is left.
-int ring_depths(MmaArgs &a) {
+// Ring depths: X stages (at least three, about 64 KiB), accumulator sets in the
+// tensor memory above the A stages, and raw stages in the shared memory left.
+int ring_depths(int type, MmaArgs &a) {
     const uint32_t x_stage = 256u * (uint32_t)a.b_pad;
-    a.nx = (int)std::min<uint32_t>(kMaxStages, std::max<uint32_t>(3u, 65536u / x_stage));
-    a.acol0 = (uint32_t)((2 * a.b_pad + 63) / 64 * 64);
-    a.na = (int)std::min<uint32_t>(kMaxStages, (kTmemCols - a.acol0) / 64);
+    (void)x_stage;
+    a.nx = kAStages;  // the X slots travel with the A stages
+    const uint32_t dset = (uint32_t)(groups_per_sub(type) * a.b_pad);
+    a.nd = (int)std::min<uint32_t>(kMaxStages, (kTmemCols - kDCol0) / dset);
+    if (a.nd < kLag + 1) return QDQ_ERR_LIMIT;
     const Layout L0 = layout_for(a.stage_bytes, 0, a.nx, a.b_pad);
     const uint32_t fixed = L0.tmem_slot + 16u;
     a.nraw = fixed >= kSmemBudget ? 0 : (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed) / a.stage_bytes);
@@ -881,22 +1047,27 @@ int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const f
     a.rows = rows;
     a.cols = cols;
     a.nunits = (int)((cols + kUnitK - 1) / kUnitK);
-    const int first = batch < kMaxBPad ? batch : kMaxBPad;
+    const int bmax = max_bpad(type);
+    const int first = batch < bmax ? batch : bmax;
     const int bpad_max = (first + 15) / 16 * 16;
+    const size_t split_bytes = (size_t)4 * bpad_max * cols;
+    const size_t sum_bytes = type == QDQ_Q4_K ? (size_t)(cols / 32) * bpad_max * sizeof(float) : 0;
     void *xs = nullptr;
-    if ((rc = scratch_alloc(&xs, (size_t)4 * bpad_max * cols, stream))) return rc;
+    if ((rc = scratch_alloc(&xs, split_bytes + sum_bytes, stream))) return rc;
     a.xs = (const uint8_t *)xs;
-    for (int b0 = 0; b0 < batch && rc == QDQ_OK; b0 += kMaxBPad) {
-        const int bc = batch - b0 < kMaxBPad ? batch - b0 : kMaxBPad;
+    a.xsum = sum_bytes ? reinterpret_cast<const float *>((const uint8_t *)xs + split_bytes) : nullptr;
+    for (int b0 = 0; b0 < batch && rc == QDQ_OK; b0 += bmax) {
+        const int bc = batch - b0 < bmax ? batch - b0 : bmax;
         a.batch = bc;
         a.b_pad = (bc + 15) / 16 * 16;
         a.y = y + (int64_t)b0 * rows;
-        if ((rc = ring_depths(a))) break;
+        if ((rc = ring_depths(type, a))) break;
         const uint32_t smem = layout_for(a.stage_bytes, a.nraw, a.nx, a.b_pad).total;
         const int S = usable_cluster(type, mma_cluster_size(rows, cols, sm_count), smem);
         const int64_t work = (cols / 16) * a.b_pad * 2;
         const int grid = (int)std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8);
-        xsplit_kernel<<<grid, 256, 0, stream>>>(x + (int64_t)b0 * cols, bc, a.b_pad, cols, (uint8_t *)xs);
+        xsplit_kernel<<<grid, 256, 0, stream>>>(x + (int64_t)b0 * cols, bc, a.b_pad, cols, (uint8_t *)xs,
+                                                const_cast<float *>(a.xsum));
         if (cudaGetLastError() != cudaSuccess) {
             rc = QDQ_ERR_CUDA;
             break;
