@@ -32,7 +32,7 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
 int take_status_stream();
 int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);
 
-// The tensor-core batched GEMV (batch >= 9).
+// The tensor-core batched GEMV (single GEMVs with batch >= kMmaMinBatch).
 int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y,
                     int batch, cudaStream_t stream, int sm_count);
 int take_status_mma();
@@ -40,6 +40,7 @@ int take_status_mma();
 constexpr int kMaxPlanDescs = 192;
 constexpr int kMaxPlanLevels = 128;
 constexpr int kMaxGroupDescs = 8;
-constexpr int kStreamMaxBatch = 8;
+constexpr int kStreamMaxBatch = 8;  // streaming kernel (plans, groups, small single GEMVs)
+constexpr int kMmaMinBatch = 4;     // single GEMVs from this batch on run on the tensor cores
 
 }  // namespace qdq

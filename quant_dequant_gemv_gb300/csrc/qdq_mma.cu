@@ -99,6 +99,9 @@ constexpr uint32_t kFinalOff = 64u * 1024u;  // per-tile result [b][128] after t
 // fit in tensor memory (Q6_K has four 16-weight groups per sub-chunk).
 __host__ __device__ constexpr int max_bpad(int type) { return type == QDQ_Q6_K ? 32 : 64; }
 __host__ __device__ constexpr int groups_per_sub(int type) { return type == QDQ_Q6_K ? 4 : 2; }
+__host__ __device__ constexpr bool stacked_b(int type, int bpad) {
+    return groups_per_sub(type) * 2 * bpad * 3 <= (int)(512 - 32 * 4);
+}
 
 struct MmaArgs {
     const uint8_t *W;   // rows x row_bytes
@@ -377,7 +380,7 @@ QDQ_DEV void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uin
         : "memory");
 }
 
-template <int TYPE>
+template <int TYPE, int BP>
 __global__ void __launch_bounds__(kThreads, 1)
     mma_gemv_kernel(const MmaArgs a, const __grid_constant__ CUtensorMap wmap) {
     constexpr int kBB = TYPE == QDQ_Q4_K ? 144 : TYPE == QDQ_Q6_K ? 210 : TYPE == QDQ_Q8_0 ? 36 : 18;
@@ -386,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kG = groups_per_sub(TYPE);         // scale groups per sub-chunk
     constexpr int kKbh = TYPE == QDQ_Q8_0 ? 4 : kUnitK / kBW;  // blocks per box row
     extern __shared__ __align__(1024) uint8_t smem[];
-    const Layout L = layout_for(a.stage_bytes, a.nraw, a.nx, a.b_pad);
+    constexpr int b_pad = BP;  // padded batch (MMA N), a compile-time constant so that every
+                               // MMA operand is a fixed offset from a uniform base
+    const Layout L = layout_for(a.stage_bytes, a.nraw, a.nx, b_pad);
     const uint32_t sb = smem_u32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int *status = &s_status_mma;
@@ -398,8 +403,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int trows = (int)(a.rows_full - row0 <= 0 ? 0 : (a.rows_full - row0 < kM ? a.rows_full - row0 : kM));
     const int nleft = rows_here - trows;
     const int u0 = (int)((int64_t)a.nunits * rank / S), u1 = (int)((int64_t)a.nunits * (rank + 1) / S);
-    const int b_pad = a.b_pad, nraw = a.nraw, nd = a.nd;
-    const uint32_t dset = (uint32_t)(kG * b_pad);  // accumulator columns of one sub-chunk
+    const int nraw = a.nraw, nd = a.nd;
+    // x_hi and x_lo as one stacked B operand (N = 2 b_pad, one MMA per K-step, the
+    // two halves summed at read-back) when three sub-chunks of such accumulators fit
+    // in tensor memory; otherwise two MMAs per K-step into the same columns
+    constexpr bool kStack = stacked_b(TYPE, BP);
+    constexpr uint32_t gcols = kStack ? 2 * b_pad : b_pad;  // accumulator columns of one group
+    constexpr uint32_t dset = (uint32_t)kG * gcols;         // ... of one sub-chunk
+    // sub-chunks of this CTA: four per full unit, fewer for a short last unit; the
+    // last sub-chunk of the matrix may have fewer than four K-steps
+    const int ns_last = u1 == a.nunits ? (unit_k(a, u1 - 1) + kSubK - 1) / kSubK : kUnitK / kSubK;
+    const int J = (u1 - u0 - 1) * (kUnitK / kSubK) + ns_last;
+    const int ks_last = u1 == a.nunits ? (unit_k(a, u1 - 1) - kSubK * (ns_last - 1)) / 16 : 4;
 
     const uint32_t raw_full = sb + L.bars, raw_empty = raw_full + 8 * kMaxStages;
     const uint32_t d_full = raw_empty + 8 * kMaxStages, d_empty = d_full + 8 * kMaxStages;
@@ -510,48 +525,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lone thread issuing from per-thread registers reaches a tenth of the rate).
         // Per K-step t of a sub-chunk: Z_g += q x_hi and Z_g += q x_lo into the
         // accumulator region of t's group.
-        const uint32_t idesc = make_idesc(b_pad);
+        const uint32_t idesc = make_idesc(b_pad), idesc2 = make_idesc(2 * b_pad);
         const uint64_t xdesc = make_sdesc(sb + L.x);  // X slot 0, K-step 0
         const uint32_t xdesc_lo = (uint32_t)xdesc, xdesc_hi = (uint32_t)(xdesc >> 32);
-        const uint32_t slot_step = L.x_stage >> 4, kstep_step = (64u * b_pad) >> 4;
-        const uint32_t lo_step = (32u * b_pad) >> 4;  // the x_lo rows follow the x_hi rows
-        Ring ra(kAStages), rd(nd);
+        constexpr uint32_t slot_step = (256u * b_pad) >> 4, kstep_step = (64u * b_pad) >> 4;
+        constexpr uint32_t lo_step = (32u * b_pad) >> 4;  // the x_lo rows follow the x_hi rows
+        int rd_s = 0, rd_p = 0, phase = 0;
         bool ok = true;
-        int j = 0;
-        for (int u = u0; u < u1 && ok; ++u) {
-            const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-            for (int sub = 0; sub < ns; ++sub, ++j, ra.next(), rd.next()) {
-                if (lane == 0 && j < 8) MTC(7, 16 + j);
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_full + 8 * ra.slot, ra.phase, status));
-                if (lane == 0) MTC(5, j);
-                if (ok && j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_empty + 8 * rd.slot, rd.phase ^ 1, status));
-                if (lane == 0) MTC(6, j);
-                if (!ok) break;
-                tc_fence_after();
-                if (lane == 0 && j < 8) MTC(7, 40 + j);
-                const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
-                const uint32_t blo = xdesc_lo + ra.slot * slot_step;
-                const uint32_t abase = tmem + 32u * ra.slot, dbase = tmem + kDCol0 + rd.slot * dset;
+        // unrolled over the four A stages: slot s is a compile-time constant
+        for (int j0 = 0; j0 < J && ok; j0 += kAStages, phase ^= 1) {
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    if (t < ks) {
-                        const uint32_t bt = blo + t * kstep_step;
-                        const uint32_t dg = dbase + ((kG == 4) ? t : (t >> 1)) * b_pad;
-                        const uint32_t acc = (kG == 4) ? 0u : (uint32_t)(t & 1);  // first write of the region
+            for (int s = 0; s < kAStages; ++s) {
+                const int j = j0 + s;
+                if (j < J && ok) {
+                    if (lane == 0 && j < 8) MTC(7, 16 + j);
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_full + 8 * s, phase, status));
+                    if (lane == 0) MTC(5, j);
+                    if (ok && j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_empty + 8 * rd_s, rd_p ^ 1, status));
+                    if (lane == 0) MTC(6, j);
+                    if (ok) {
+                        tc_fence_after();
+                        if (lane == 0 && j < 8) MTC(7, 40 + j);
+                        const int ks = j == J - 1 ? ks_last : 4;
+                        const uint32_t dbase = tmem + kDCol0 + (uint32_t)rd_s * dset;
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            if (t < ks) {
+                                const uint32_t bt = xdesc_lo + s * slot_step + t * kstep_step;
+                                const uint32_t dg = dbase + ((kG == 4) ? t : (t >> 1)) * gcols;
+                                const uint32_t acc = (kG == 4) ? 0u : (uint32_t)(t & 1);  // region's first write
+                                if (elect_one()) {
+                                    if constexpr (kStack) {
+                                        mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt, xdesc_hi), idesc2, acc);
+                                    } else {
+                                        mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt, xdesc_hi), idesc, acc);
+                                        mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt + lo_step, xdesc_hi), idesc,
+                                               1u);
+                                    }
+                                }
+                                __syncwarp();
+                            }
+                        }
+                        if (lane == 0 && j < 8) MTC(7, 32 + j);
                         if (elect_one()) {
-                            mma_ts(dg, abase + 8 * t, desc_from_words(bt, xdesc_hi), idesc, acc);
-                            mma_ts(dg, abase + 8 * t, desc_from_words(bt + lo_step, xdesc_hi), idesc, 1u);
+                            mma_commit(a_empty + 8 * s);
+                            mma_commit(d_full + 8 * rd_s);
                         }
                         __syncwarp();
+                        if (lane == 0 && j < 8) MTC(7, 24 + j);
+                        if (++rd_s == nd) {
+                            rd_s = 0;
+                            rd_p ^= 1;
+                        }
                     }
                 }
-                if (lane == 0 && j < 8) MTC(7, 32 + j);
-                if (elect_one()) {
-                    mma_commit(a_empty + 8 * ra.slot);
-                    mma_commit(d_full + 8 * rd.slot);
-                }
-                __syncwarp();
-                if (lane == 0 && j < 8) MTC(7, 24 + j);
             }
         }
     } else {
@@ -594,12 +621,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * rd_slot(), rd_phase(), status))) return false;
             if (lane == 0 && dw < 8 && rd_count < 8) MTC(3, dw * 8 + rd_count);
             tc_fence_after();
-            const uint32_t dcol = tl + kDCol0 + (uint32_t)rd_slot() * dset + grp * b_pad + col0;
+            const uint32_t dcol = tl + kDCol0 + (uint32_t)rd_slot() * dset + grp * gcols + col0;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
                 if (8 * c8 < cw) {
                     uint32_t v[8];
                     tmem_ld8(dcol + 8 * c8, v);
+                    float z[8];
+                    if constexpr (kStack) {
+                        uint32_t w[8];
+                        tmem_ld8(dcol + b_pad + 8 * c8, w);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) z[t] = __uint_as_float(v[t]) + __uint_as_float(w[t]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) z[t] = __uint_as_float(v[t]);
+                    }
                     if (gg >= 0) {
                         if constexpr (TYPE == QDQ_Q4_K) {
                             const float4 *xg =
@@ -607,12 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float4 x0 = __ldg(xg), x1 = __ldg(xg + 1);
                             const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-                            for (int t = 0; t < 8; ++t)
-                                yacc[8 * c8 + t] = fmaf(sc, __uint_as_float(v[t]), fmaf(-mn, xv[t], yacc[8 * c8 + t]));
+                            for (int t = 0; t < 8; ++t) yacc[8 * c8 + t] = fmaf(sc, z[t], fmaf(-mn, xv[t], yacc[8 * c8 + t]));
                         } else {
 #pragma unroll
-                            for (int t = 0; t < 8; ++t)
-                                yacc[8 * c8 + t] = fmaf(sc, __uint_as_float(v[t]), yacc[8 * c8 + t]);
+                            for (int t = 0; t < 8; ++t) yacc[8 * c8 + t] = fmaf(sc, z[t], yacc[8 * c8 + t]);
                         }
                     }
                 }
@@ -626,9 +661,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
 
-        // sub-chunks of this CTA: four per full unit, fewer for a short last unit
-        const int J = (u1 - u0) * (kUnitK / kSubK) -
-                      (u1 == a.nunits ? (kUnitK / kSubK) - (unit_k(a, u1 - 1) + kSubK - 1) / kSubK : 0);
         Ring rs(nraw), ra(kAStages);
         bool ok = true;
         int u = u0, sub = 0, ns = 0, uk = 0;
@@ -879,7 +911,7 @@ int ring_depths(int type, MmaArgs &a) {
     const uint32_t x_stage = 256u * (uint32_t)a.b_pad;
     (void)x_stage;
     a.nx = kAStages;  // the X slots travel with the A stages
-    const uint32_t dset = (uint32_t)(groups_per_sub(type) * a.b_pad);
+    const uint32_t dset = (uint32_t)(groups_per_sub(type) * a.b_pad * (stacked_b(type, a.b_pad) ? 2 : 1));
     a.nd = (int)std::min<uint32_t>(kMaxStages, (kTmemCols - kDCol0) / dset);
     if (a.nd < kLag + 1) return QDQ_ERR_LIMIT;
     const Layout L0 = layout_for(a.stage_bytes, 0, a.nx, a.b_pad);
@@ -888,7 +920,7 @@ int ring_depths(int type, MmaArgs &a) {
     return a.nraw >= 2 ? QDQ_OK : QDQ_ERR_LIMIT;
 }
 
-template <int TYPE>
+template <int TYPE, int BP>
 int launch_typed(const MmaArgs &a, const CUtensorMap &map, int S, int64_t tiles, cudaStream_t stream) {
     const Layout L = layout_for(a.stage_bytes, a.nraw, a.nx, a.b_pad);
     static std::mutex mu;
@@ -898,7 +930,7 @@ int launch_typed(const MmaArgs &a, const CUtensorMap &map, int S, int64_t tiles,
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[dev]) {
-            if (cudaFuncSetAttribute(mma_gemv_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(mma_gemv_kernel<TYPE, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      227 * 1024) != cudaSuccess)
                 return QDQ_ERR_CUDA;
             attr_set[dev] = true;
@@ -916,7 +948,7 @@ int launch_typed(const MmaArgs &a, const CUtensorMap &map, int S, int64_t tiles,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = S > 1 ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, mma_gemv_kernel<TYPE>, a, map) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, mma_gemv_kernel<TYPE, BP>, a, map) != cudaSuccess) {
         cudaGetLastError();
         return QDQ_ERR_CUDA;
     }
@@ -925,7 +957,8 @@ int launch_typed(const MmaArgs &a, const CUtensorMap &map, int S, int64_t tiles,
 
 template <int TYPE>
 int max_active_clusters(int S, uint32_t smem) {
-    if (cudaFuncSetAttribute(mma_gemv_kernel<TYPE>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+    // every b_pad instantiation has the same launch shape; the 16-column one stands for all
+    if (cudaFuncSetAttribute(mma_gemv_kernel<TYPE, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
         cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -942,19 +975,34 @@ int max_active_clusters(int S, uint32_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mma_gemv_kernel<TYPE>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, mma_gemv_kernel<TYPE, 16>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
 }
 
+template <int TYPE>
+int dispatch_bp(const MmaArgs &a, const CUtensorMap &map, int S, int64_t tiles, cudaStream_t stream) {
+    switch (a.b_pad) {
+        case 16: return launch_typed<TYPE, 16>(a, map, S, tiles, stream);
+        case 32: return launch_typed<TYPE, 32>(a, map, S, tiles, stream);
+        case 48:
+            if constexpr (max_bpad(TYPE) >= 48) return launch_typed<TYPE, 48>(a, map, S, tiles, stream);
+            return QDQ_ERR_LIMIT;
+        case 64:
+            if constexpr (max_bpad(TYPE) >= 64) return launch_typed<TYPE, 64>(a, map, S, tiles, stream);
+            return QDQ_ERR_LIMIT;
+        default: return QDQ_ERR_LIMIT;
+    }
+}
+
 int dispatch(int type, const MmaArgs &a, const CUtensorMap &map, int S, int64_t tiles, cudaStream_t stream) {
     switch (type) {
-        case QDQ_Q4_K: return launch_typed<QDQ_Q4_K>(a, map, S, tiles, stream);
-        case QDQ_Q6_K: return launch_typed<QDQ_Q6_K>(a, map, S, tiles, stream);
-        case QDQ_Q8_0: return launch_typed<QDQ_Q8_0>(a, map, S, tiles, stream);
-        case QDQ_Q4_0: return launch_typed<QDQ_Q4_0>(a, map, S, tiles, stream);
+        case QDQ_Q4_K: return dispatch_bp<QDQ_Q4_K>(a, map, S, tiles, stream);
+        case QDQ_Q6_K: return dispatch_bp<QDQ_Q6_K>(a, map, S, tiles, stream);
+        case QDQ_Q8_0: return dispatch_bp<QDQ_Q8_0>(a, map, S, tiles, stream);
+        case QDQ_Q4_0: return dispatch_bp<QDQ_Q4_0>(a, map, S, tiles, stream);
         default: return QDQ_ERR_TYPE;
     }
 }
@@ -1034,7 +1082,7 @@ int mma_cluster_size(int64_t rows, int64_t cols, int sm_count) {
 
 int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y, int batch,
                     cudaStream_t stream, int sm_count) {
-    if (batch <= kStreamMaxBatch) return QDQ_ERR_LIMIT;
+    if (batch < kMmaMinBatch) return QDQ_ERR_LIMIT;
     const int64_t tiles = (rows + kM - 1) / kM;
     if (tiles > 65535) return QDQ_ERR_LIMIT;
     if (qdq_block_weights(type) <= 0) return QDQ_ERR_TYPE;
