@@ -431,13 +431,15 @@ def main():
             "config": {"workload": WORKLOADS[args.workload], "batch": args.batch,
                        "step_bytes": abytes,
                        "l2": ("inputs larger than L2 (weights per step exceed 129 MB)" if args.workload == "step"
-                              else "weights rotate over copies totalling at least 4x the 129 MB L2")
-                       if abytes > 4 * 129e6 else "inputs smaller than L2: figures include L2 hits",
+                              else "weights rotate over copies totalling at least 4x the 129 MB L2; "
+                                   "timed steps replay CUDA graphs of the qdq_gemv calls"),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic, "peak_source": peaks["source"],
-                         "kernel": "stream_kernel (persistent plan launch)"},
+                         "kernel": ("stream_kernel (persistent plan launch)" if args.workload == "step"
+                                    else "mma_gemv_kernel + xsplit_kernel (tensor cores)"
+                                    if args.batch >= MMA_MIN_BATCH else "stream_kernel (one GEMV per launch)")},
             "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": r["launches"],
