@@ -341,6 +341,23 @@ def time_oracle(levels, batch, budget_s):
     return spent, done_bytes, n
 
 
+def slowest_replica(total_ms: float, e2e_s: float, world: int, device) -> tuple[float, float]:
+    """Replicas (one process per GPU, no data exchange): the job's time is the
+    slowest rank's. Uses the initialised process group (NCCL on GPUs, gloo in tests)."""
+    if world <= 1:
+        return total_ms, e2e_s
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([total_ms, e2e_s], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0]), float(t[1])
+
+
+def replicas_gbs(step_bytes: int, world: int, ms_step: float) -> float:
+    """Whole-job throughput: every replica moves step_bytes per step."""
+    return world * step_bytes / (ms_step * 1e-3) / 1e9
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -400,16 +417,9 @@ def main():
     torch.cuda.set_device(device)
     r = run_ours(args, rank, world, device)
 
-    total_ms = r["total_ms"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, r["e2e_s"]], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_s = float(t[0]), float(t[1])
-    else:
-        e2e_s = r["e2e_s"]
+    total_ms, e2e_s = slowest_replica(r["total_ms"], r["e2e_s"], world, device)
     ms_step = total_ms / args.steps
-    value = world * abytes / (ms_step * 1e-3) / 1e9
+    value = replicas_gbs(abytes, world, ms_step)
     avg_launch_ms = statistics.mean(r["launch_ms"])
     achieved = abytes / (avg_launch_ms * 1e-3) / 1e9
     peaks = load_peaks()
