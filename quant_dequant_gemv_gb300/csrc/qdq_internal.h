@@ -37,6 +37,18 @@ int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const f
                     int batch, cudaStream_t stream, int sm_count);
 int take_status_mma();
 
+// While a caller's stream is being captured into a CUDA graph, one-time setup calls
+// (kernel attributes, occupancy queries, memory-pool creation) would invalidate a
+// capture in global mode; this scope relaxes the calling thread's capture mode for
+// them. Stream operations issued inside it are still captured.
+struct RelaxedCaptureScope {
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    RelaxedCaptureScope() { cudaThreadExchangeStreamCaptureMode(&mode); }
+    ~RelaxedCaptureScope() { cudaThreadExchangeStreamCaptureMode(&mode); }
+    RelaxedCaptureScope(const RelaxedCaptureScope &) = delete;
+    RelaxedCaptureScope &operator=(const RelaxedCaptureScope &) = delete;
+};
+
 constexpr int kMaxPlanDescs = 192;
 constexpr int kMaxPlanLevels = 128;
 constexpr int kMaxGroupDescs = 8;

@@ -1083,6 +1083,7 @@ int mma_cluster_size(int64_t rows, int64_t cols, int sm_count) {
 int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y, int batch,
                     cudaStream_t stream, int sm_count) {
     if (batch < kMmaMinBatch) return QDQ_ERR_LIMIT;
+    RelaxedCaptureScope relaxed;  // first-use setup may run inside a caller's graph capture
     const int64_t tiles = (rows + kM - 1) / kM;
     if (tiles > 65535) return QDQ_ERR_LIMIT;
     if (qdq_block_weights(type) <= 0) return QDQ_ERR_TYPE;

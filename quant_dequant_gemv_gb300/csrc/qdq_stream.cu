@@ -1021,6 +1021,7 @@ static int bt_of(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 
 template <int BT, int MAXD, int MAXL>
 static int launch_typed(const StreamPlanHost *p, cudaStream_t stream) {
     auto kern = stream_kernel<BT, MAXD, MAXL>;
+    RelaxedCaptureScope relaxed;  // the first launch sets the kernel's attributes
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
