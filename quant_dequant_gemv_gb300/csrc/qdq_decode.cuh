@@ -55,7 +55,9 @@ QDQ_DEV uint32_t q6k_quant_bytes(uint32_t ql, uint32_t qh, int k) {
         case 2: high = qh; break;
         default: high = qh >> 2; break;
     }
-    return low | (high & 0x30303030u);
+    uint32_t q6;  // low | (high & 0x30303030) as one LOP3
+    asm("lop3.b32 %0, %1, %2, %3, 0xF8;" : "=r"(q6) : "r"(low), "r"(high), "n"(0x30303030));
+    return q6;
 }
 
 // ---- exact per-weight values (for the dequantisation kernel) ---------------------

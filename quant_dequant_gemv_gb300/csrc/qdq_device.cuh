@@ -175,6 +175,16 @@ QDQ_DEV uint64_t fsub2(uint64_t a, uint64_t b) {
 }
 QDQ_DEV uint64_t bits2(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
 
+// (v & MASK) | 0x4B000000 in one LOP3. Written as C, the mask-then-or costs two
+// ALU-pipe instructions per weight, and the ALU pipe (half the FMA pipe's rate)
+// is what bounds the batch-1 nibble loops.
+template <uint32_t MASK>
+QDQ_DEV uint32_t mask_magic(uint32_t v) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(v), "n"(MASK), "n"(0x4B000000));
+    return d;
+}
+
 // fp16 bit pattern -> fp32 (exact; the conversion the format's scales need).
 QDQ_DEV float half_bits_to_float(uint32_t h16) { return __half2float(__ushort_as_half((unsigned short)h16)); }
 

@@ -358,10 +358,10 @@ QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, co
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const uint32_t v = w[t], u = v >> 16;
-                a0 = ffma2(fsub2(bits2((v & 0xFu) | kMagic, (v & 0xF00u) | kMagic), M2), xr.v[2 * t], a0);
-                a1 = ffma2(fsub2(bits2((v & 0xF0000u) | kMagic, (u & 0xF00u) | kMagic), M2), xr.v[2 * t + 1], a1);
-                h0 = ffma2(fsub2(bits2((v & 0xF0u) | kMagic, (v & 0xF000u) | kMagic), M2), xr.v[16 + 2 * t], h0);
-                h1 = ffma2(fsub2(bits2((u & 0xF0u) | kMagic, (u & 0xF000u) | kMagic), M2), xr.v[17 + 2 * t], h1);
+                a0 = ffma2(fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2), xr.v[2 * t], a0);
+                a1 = ffma2(fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2), xr.v[2 * t + 1], a1);
+                h0 = ffma2(fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2), xr.v[16 + 2 * t], h0);
+                h1 = ffma2(fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2), xr.v[17 + 2 * t], h1);
             }
             const float lo = (lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1));
             const float hi = (lo_of(h0) + hi_of(h0)) + (lo_of(h1) + hi_of(h1));
@@ -371,10 +371,10 @@ QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, co
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const uint32_t v = w[t], u = v >> 16;
-                q[2 * t] = fsub2(bits2((v & 0xFu) | kMagic, (v & 0xF00u) | kMagic), M2);
-                q[2 * t + 1] = fsub2(bits2((v & 0xF0000u) | kMagic, (u & 0xF00u) | kMagic), M2);
-                q[16 + 2 * t] = fsub2(bits2((v & 0xF0u) | kMagic, (v & 0xF000u) | kMagic), M2);
-                q[17 + 2 * t] = fsub2(bits2((u & 0xF0u) | kMagic, (u & 0xF000u) | kMagic), M2);
+                q[2 * t] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2);
+                q[2 * t + 1] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2);
+                q[16 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2);
+                q[17 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2);
             }
 #pragma unroll
             for (int b = 0; b < BT; ++b) {
@@ -562,10 +562,10 @@ QDQ_DEV void unit_q4_0(const uint8_t *const *wrow, int lane, int nblk_valid, con
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const uint32_t v = qs[4 * i + t], u = v >> 16;
-                q[16 * i + 2 * t] = fsub2(bits2((v & 0xFu) | kMagic, (v & 0xF00u) | kMagic), C_la);
-                q[16 * i + 2 * t + 1] = fsub2(bits2((v & 0xF0000u) | kMagic, (u & 0xF00u) | kMagic), C_lb);
-                q[16 * i + 8 + 2 * t] = fsub2(bits2((v & 0xF0u) | kMagic, (v & 0xF000u) | kMagic), C_h);
-                q[16 * i + 9 + 2 * t] = fsub2(bits2((u & 0xF0u) | kMagic, (u & 0xF000u) | kMagic), C_h);
+                q[16 * i + 2 * t] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), C_la);
+                q[16 * i + 2 * t + 1] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), C_lb);
+                q[16 * i + 8 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), C_h);
+                q[16 * i + 9 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), C_h);
             }
         }
 #pragma unroll
