@@ -318,8 +318,9 @@ int qdq_get_device_status(qdq_stream_t stream) {
         return QDQ_ERR_CUDA;
     }
     const int a = take_status_stream();
+    const int a1 = take_status_stream1();
     const int b = take_status_mma();
-    return a != QDQ_OK ? a : b;
+    return a != QDQ_OK ? a : a1 != QDQ_OK ? a1 : b;
 }
 
 int qdq_selftest_wait_timeout(int64_t timeout_ns, qdq_stream_t stream) {

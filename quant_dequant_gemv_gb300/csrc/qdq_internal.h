@@ -30,6 +30,9 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
                                  unsigned *counters, int sm_count, cudaStream_t stream);
 
 int take_status_stream();
+// Batch-1 streaming kernel (qdq_stream1.cu): takes the same packed arguments.
+int stream1_launch(const void *args, bool big, bool cooperative, int grid, cudaStream_t stream);
+int take_status_stream1();
 int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);
 
 // The tensor-core batched GEMV (single GEMVs with batch >= kMmaMinBatch).
