@@ -204,6 +204,35 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
     }
 }
 
+// Rows [ra, rb) of GEMV g that CTA `cta` owns in level L. The level's CTAs are
+// dealt out to its GEMVs in proportion to their weight bytes (rounded CTA
+// boundaries over the cumulative bytes), and each GEMV's rows are split evenly
+// among its CTAs, so a CTA normally works on a single GEMV per level: one x
+// format and as few tiles as possible. A GEMV too small to earn a CTA of its own
+// goes whole to the CTA at its position.
+template <class A>
+QDQ_DEV void cta_rows_by_gemv(const A &a, int L, int g, int cta, int P, int64_t *ra, int64_t *rb) {
+    int64_t total = 0, before = 0;
+    for (int i = a.level_start[L]; i < a.level_start[L + 1]; ++i) {
+        const int64_t bytes = a.d[i].rows * (int64_t)a.d[i].rb;
+        if (i < g) before += bytes;
+        total += bytes;
+    }
+    const int64_t mine = a.d[g].rows * (int64_t)a.d[g].rb, rows = a.d[g].rows;
+    *ra = *rb = 0;
+    if (total <= 0 || rows <= 0) return;
+    const int c0 = (int)((before * P + total / 2) / total);
+    const int c1 = (int)(((before + mine) * P + total / 2) / total);
+    if (c1 <= c0) {  // no CTA of its own
+        if (cta == (c0 < P ? c0 : P - 1)) *rb = rows;
+        return;
+    }
+    if (cta < c0 || cta >= c1) return;
+    const int64_t n = c1 - c0, l = cta - c0;
+    *ra = l * rows / n;
+    *rb = (l + 1) * rows / n;
+}
+
 // Byte offset of chunk j inside a row, and the shared-memory address of row
 // `row`'s segment of the tile in a stage (it keeps the source's offset mod 16).
 QDQ_DEV int64_t chunk_off(const DevDesc &d, int j) {
@@ -450,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
     }
     for (int L = 0; L < a.nlevels; ++L)
         for (int g = a.level_start[L] + (int)threadIdx.x; g < a.level_start[L + 1]; g += kThreads)
-            cta_rows(a, L, g, cta, P, &ranges[2 * g], &ranges[2 * g + 1]);
+            cta_rows_by_gemv(a, L, g, cta, P, &ranges[2 * g], &ranges[2 * g + 1]);
     __syncthreads();
 
     if (warp == 0) {
