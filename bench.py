@@ -49,9 +49,9 @@ WORKLOADS = {
 }
 
 
-def workload_levels(name: str) -> list[list[synth.Gemv]]:
+def workload_levels(name: str, layers: int = 22) -> list[list[synth.Gemv]]:
     if name == "step":
-        return synth.llama_1b_step(22)
+        return synth.llama_1b_step(layers)
     if name == "q4k":
         return [[synth.Q4K_2048x2048]]
     if name == "q6k":
@@ -192,7 +192,7 @@ def run_ours(args, rank, world, device):
     from quant_dequant_gemv_gb300 import build, qdq
 
     build.build()
-    levels = workload_levels(args.workload)
+    levels = workload_levels(args.workload, args.layers)
     batch = args.batch
     stream = torch.cuda.current_stream(device)
     abytes = algorithmic_bytes(levels, batch)
@@ -367,6 +367,8 @@ def main():
     ap.add_argument("--workload", default="step", choices=sorted(WORKLOADS))
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=22,
+                    help="layers of the decode-step workload (a shorter step for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -374,9 +376,14 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    levels = workload_levels(args.workload)
+    levels = workload_levels(args.workload, args.layers)
     abytes = algorithmic_bytes(levels, args.batch)
     step_bytes = abytes
+    wname = WORKLOADS[args.workload]
+    tkey = args.workload
+    if args.workload == "step" and args.layers != 22:
+        wname = f"{args.layers}-layer variant of the " + wname
+        tkey = f"step{args.layers}"
 
     if args.impl == "reference":
         # The reference arm is the CPU oracle, as it stands, on the host cores:
@@ -399,7 +406,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * spent / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 (oracle: f64 sums)",
             "data": "synthetic", "tok_s": round(gbs * 1e9 / step_bytes, 4),
-            "config": {"workload": WORKLOADS[args.workload], "batch": args.batch,
+            "config": {"workload": wname, "batch": args.batch,
                        "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"first {n_last} GEMVs of the workload in step order per step "
@@ -423,7 +430,7 @@ def main():
     avg_launch_ms = statistics.mean(r["launch_ms"])
     achieved = abytes / (avg_launch_ms * 1e-3) / 1e9
     peaks = load_peaks()
-    traffic = recorded_traffic(args.workload, args.batch)
+    traffic = recorded_traffic(tkey, args.batch)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -438,7 +445,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "tok_s": round(world * 1e3 / ms_step, 1),
-            "config": {"workload": WORKLOADS[args.workload], "batch": args.batch,
+            "config": {"workload": wname, "batch": args.batch,
                        "step_bytes": abytes,
                        "l2": ("inputs larger than L2 (weights per step exceed 129 MB)" if args.workload == "step"
                               else "weights rotate over copies totalling at least 4x the 129 MB L2; "
