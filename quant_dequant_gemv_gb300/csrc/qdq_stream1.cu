@@ -66,8 +66,9 @@ constexpr int kTileRows = 32;                     // rows of a whole-row tile (u
 constexpr int kChunkRows = 16;                    // rows of a chunked tile
 constexpr int kChunk = 2048;                      // columns of a chunk: kCW slices of kSlice
 constexpr int kSlice = 256;
-constexpr int kNST = 4;                           // ring stages
-constexpr int kStageBytes = 43008;                // 32 Q4_K rows of 2048 columns (+ slack)
+constexpr int kRingBytes = 172032;                // W ring: tiles packed in order, wrapping
+constexpr int kMaxTileBytes = kRingBytes / 2;     // at least two tiles in flight
+constexpr int kSlots = 8;                         // full/empty barrier pairs (tiles in the ring)
 constexpr int kXFloats = 1024;                    // private x area of one consumer warp
 constexpr int kBufRows = 512;                     // rows of the level partial buffer
 constexpr int kFlushBar = 1;                      // named barrier of the consumer warps
@@ -75,12 +76,13 @@ constexpr int kFlushBar = 1;                      // named barrier of the consum
 // Shared memory layout (bytes). The ring starts at 0 (1024-aligned base).
 template <int MAXD>
 struct Smem {
-    static constexpr int kX = kNST * kStageBytes;
+    static constexpr int kX = kRingBytes;
     static constexpr int kPart = kX + kCW * kXFloats * 4;     // [warp][buffer row] partials
     static constexpr int kDst = kPart + kCW * kBufRows * 4;   // y address of each buffer row
     static constexpr int kRanges = kDst + kBufRows * 8;
-    static constexpr int kBars = kRanges + 2 * MAXD * 8;
-    static constexpr int kBytes = kBars + (2 * kNST + 2) * 8;
+    static constexpr int kRing = kRanges + 2 * MAXD * 8;      // producer: live tiles' ring ranges
+    static constexpr int kBars = kRing + 2 * kSlots * 4;
+    static constexpr int kBytes = kBars + (2 * kSlots + 2) * 8;
 };
 static_assert(Smem<kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
 
@@ -119,13 +121,28 @@ QDQ_DEV int seg_pitch(int seg) { return ((seg + 15) & ~15) + 16; }
 // rows fit a stage or the row's x does not fit one window.
 QDQ_DEV int whole_rows(const DevDesc &d) {
     const int nch = (d.cols + kChunk - 1) / kChunk;
-    const int cap = (kStageBytes - 32) / d.rb;
+    const int cap = (kMaxTileBytes - 32) / d.rb;
     if (cap < 8 || nch > window_chunks(d.kinds)) return 0;
     return cap >= kTileRows ? kTileRows : cap & ~7;
 }
 QDQ_DEV int chunk_rows(const DevDesc &d) {
-    const int cap = kStageBytes / seg_pitch(seg_bytes(d, kChunk));
+    const int cap = kMaxTileBytes / seg_pitch(seg_bytes(d, kChunk));
     return cap < kChunkRows ? (cap < 1 ? 1 : cap) : kChunkRows;
+}
+
+// Bytes a tile takes in the ring (copy_span may start up to 15 bytes before and
+// end up to 15 bytes after the tile's rows; chunk segments sit at their pitch).
+QDQ_DEV uint32_t tile_ring_bytes(const DevDesc &d, int nrows, bool whole, int ccols) {
+    const uint32_t b = whole ? (uint32_t)(nrows * d.rb + 32) : (uint32_t)(nrows * seg_pitch(seg_bytes(d, ccols)));
+    return (b + 127u) & ~127u;
+}
+// Next tile's offset in the ring: packed after the previous one, or at 0 when it
+// would not fit before the end. Producer and consumers run the same sequence.
+QDQ_DEV uint32_t ring_place(uint32_t &next, uint32_t bytes) {
+    if (next + bytes > (uint32_t)kRingBytes) next = 0;
+    const uint32_t o = next;
+    next += bytes;
+    return o;
 }
 
 // on_begin(L) / on_end(L) around each level; on_tile(tile, epoch, desc) for every
@@ -458,10 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
     uint64_t *dst = (uint64_t *)(smem + SM::kDst);
     int64_t *ranges = (int64_t *)(smem + SM::kRanges);
     const uint32_t ring_a = smem_u32(smem);
-    const uint32_t full_a = smem_u32(smem + SM::kBars), empty_a = full_a + 8 * kNST;
+    const uint32_t full_a = smem_u32(smem + SM::kBars), empty_a = full_a + 8 * kSlots;
     // lvl: this CTA's consumers finished a level; dep: every CTA finished the
     // previous level (arrival by the control warp).
-    const uint32_t lvl_a = empty_a + 8 * kNST, dep_a = lvl_a + 8;
+    const uint32_t lvl_a = empty_a + 8 * kSlots, dep_a = lvl_a + 8;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x, P = gridDim.x;
@@ -469,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
     const bool levels_synced = a.counters != nullptr;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNST; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(full_a + 8 * s, 1);
             mbar_init(empty_a + 8 * s, kCW);
         }
@@ -485,21 +502,39 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        int t = 0;
+        // A tile takes the next ring bytes; before copying, the producer waits (in
+        // FIFO order) for the release of every live tile that overlaps them and of
+        // the tile that last used the barrier slot.
+        int t = 0, rel = 0;
+        uint32_t next = 0;
+        uint32_t *toff = (uint32_t *)(smem + SM::kRing), *tlen = toff + kSlots;
         walk(
             a, ranges, [](int) {},
             [&](const Tile &tl, int, const DevDesc &d) {
-                const int s = t % kNST;
-                if (t >= kNST) mbar_wait(empty_a + 8 * s, ((t / kNST) + 1) & 1, status);
-                const uint32_t stage = ring_a + s * kStageBytes, bar = full_a + 8 * s;
-                const uint32_t bytes = tile_copy(d, tl, stage, bar, kTail);
-                mbar_arrive_expect_tx(bar, bytes);  // releases the tail stores above
+                const uint32_t bytes = tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols);
+                const uint32_t o = ring_place(next, bytes);
+                for (;;) {
+                    bool block = rel < t && rel <= t - kSlots;
+                    for (int j = rel; !block && j < t; ++j) {
+                        const uint32_t jo = toff[j % kSlots], je = jo + tlen[j % kSlots];
+                        block = o < je && jo < o + bytes;
+                    }
+                    if (!block) break;
+                    mbar_wait(empty_a + 8 * (rel % kSlots), (rel / kSlots) & 1, status);
+                    ++rel;
+                }
+                const int s = t % kSlots;
+                toff[s] = o;
+                tlen[s] = bytes;
+                const uint32_t stage = ring_a + o, bar = full_a + 8 * s;
+                const uint32_t nb = tile_copy(d, tl, stage, bar, kTail);
+                mbar_arrive_expect_tx(bar, nb);  // releases the tail stores above
                 tile_copy(d, tl, stage, bar, kBulk);
                 ++t;
             },
             [](int) {});
-        for (int i = t - kNST > 0 ? t - kNST : 0; i < t; ++i)  // no exit with copies in flight
-            mbar_wait(full_a + 8 * (i % kNST), (i / kNST) & 1, status);
+        for (int i = t - kSlots > 0 ? t - kSlots : 0; i < t; ++i)  // no exit with copies in flight
+            mbar_wait(full_a + 8 * (i % kSlots), (i / kSlots) & 1, status);
         return;
     }
 
@@ -553,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
     float *mypart = part + cw * kBufRows;
     int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0, dep_phase = 0;
     int buf_rows = 0, rg_base = 0;
+    uint32_t ring_next = 0;
     bool had_tiles = false, dep_pending = false;
     (void)cur_level;
 
@@ -601,14 +637,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
             }
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 5);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 8 + 3 * tiles_in_level);
-            const int s = t % kNST;
-            mbar_wait(full_a + 8 * s, (t / kNST) & 1, status);
+            const uint32_t toffs = ring_place(ring_next, tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols));
+            const int s = t % kSlots;
+            mbar_wait(full_a + 8 * s, (t / kSlots) & 1, status);
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 6);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 9 + 3 * tiles_in_level);
             ++tiles_in_level;
 
             {
-                const uint8_t *stage_p = smem + s * kStageBytes;
+                const uint8_t *stage_p = smem + toffs;
                 RowGeo geo;
                 geo.rb = d.rb;
                 if (tl.whole) {
