@@ -62,7 +62,7 @@ constexpr int kCW = 8;                            // consumer warps
 constexpr int kFirstCW = 2;                       // warp 0 producer, warp 1 control
 constexpr int kThreads = 32 * (kCW + kFirstCW);
 constexpr int kPassRows = 16;                     // rows of one pass (lanes cover r and r + 8)
-constexpr int kTileRows = 32;                     // rows of a whole-row tile (up to two passes)
+constexpr int kTileRows = 64;                     // rows of a whole-row tile (up to four passes)
 constexpr int kChunkRows = 16;                    // rows of a chunked tile
 constexpr int kChunk = 2048;                      // columns of a chunk: kCW slices of kSlice
 constexpr int kSlice = 256;
@@ -88,13 +88,13 @@ static_assert(Smem<kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget")
 
 // ---------------------------------------------------------------------------
 // Tiles: identical sequence for the producer, the control warp and consumers.
-// A whole-row tile holds up to 32 complete rows (one contiguous bulk copy) and
+// A whole-row tile holds up to 64 complete rows (one contiguous bulk copy) and
 // every chunk of their x; rows too long for 8 per stage are cut into 2048-column
 // chunks of up to 16 rows, copied row segment by row segment.
 // ---------------------------------------------------------------------------
 struct Tile {
     int g;            // GEMV (desc index)
-    int nrows;        // 1..32 (whole rows) or 1..16 (chunked)
+    int nrows;        // 1..64 (whole rows) or 1..16 (chunked)
     int64_t row0;
     int chunk;        // chunked: the 2048-column chunk; whole rows: 0
     int ccols;        // columns of the tile (whole rows: all of them)
@@ -117,7 +117,7 @@ QDQ_DEV int window_chunks(int kinds) {
 // Bytes of one row segment of a chunk, and the stage pitch of such segments.
 QDQ_DEV int seg_bytes(const DevDesc &d, int ccols) { return (ccols / blk_weights(d.type)) * blk_bytes(d.type); }
 QDQ_DEV int seg_pitch(int seg) { return ((seg + 15) & ~15) + 16; }
-// Rows of a whole-row tile (a multiple of 8 up to 32), or 0 when fewer than 8
+// Rows of a whole-row tile (a multiple of 8 up to 64), or 0 when fewer than 8
 // rows fit a stage or the row's x does not fit one window.
 QDQ_DEV int whole_rows(const DevDesc &d) {
     const int nch = (d.cols + kChunk - 1) / kChunk;
@@ -632,8 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                 if (buf_rows + tl.nrows > kBufRows || (!tl.first_win && buf_rows > 0)) flush();
                 rg_base = buf_rows;
                 buf_rows += tl.nrows;
-                if (cw == 0 && lane < tl.nrows)
-                    dst[rg_base + lane] = (uint64_t)(uintptr_t)(d.y + tl.row0 + lane) | (tl.first_win ? 0u : 1u);
+                if (cw == 0)
+                    for (int i = lane; i < tl.nrows; i += 32)
+                        dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) | (tl.first_win ? 0u : 1u);
             }
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 5);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 8 + 3 * tiles_in_level);
