@@ -161,15 +161,23 @@ class ClockSampler:
 # our arm
 # ---------------------------------------------------------------------------
 def build_inputs(levels, batch, device, seed=0):
+    """Weights per GEMV; the activations live in two arenas (every level's x, then
+    every y, back to back in plan order), as a serving engine lays them out, so the
+    plan's host<->device transfers are one copy each way."""
     import torch
-    items, lv, xs_host = [], [], []
+    items, lv = [], []
+    xs_host = [synth.gen_x(batch, level[0].cols, seed + 1000 + li) for li, level in enumerate(levels)]
+    x_all = torch.from_numpy(np.concatenate([a.reshape(-1) for a in xs_host])).to(device)
+    y_all = torch.empty(sum(batch * g.rows for level in levels for g in level), dtype=torch.float32, device=device)
+    xo = yo = 0
     for li, level in enumerate(levels):
-        x = synth.gen_x(batch, level[0].cols, seed + 1000 + li)
-        xs_host.append(x)
-        xd = torch.from_numpy(x).to(device)
+        nx = batch * level[0].cols
+        xd = x_all[xo:xo + nx].view(batch, level[0].cols)
+        xo += nx
         for gi, g in enumerate(level):
             W = synth.gen_matrix(g.qtype, g.rows, g.cols, seed + 10 * li + gi)
-            y = torch.empty(batch, g.rows, dtype=torch.float32, device=device)
+            y = y_all[yo:yo + batch * g.rows].view(batch, g.rows)
+            yo += batch * g.rows
             items.append((g.qtype, torch.from_numpy(W).to(device), g.rows, g.cols, xd, y))
             lv.append(li)
     return items, lv, xs_host
