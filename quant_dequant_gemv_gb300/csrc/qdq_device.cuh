@@ -83,6 +83,23 @@ QDQ_DEV bool mbar_wait(uint32_t bar, uint32_t parity, int *status) {
     }
 }
 
+// Bounded wait that keeps polling (no suspension): for the level handshakes,
+// where the waiter has nothing else to do and reacting late costs the whole GPU.
+QDQ_DEV bool mbar_wait_spin(uint32_t bar, uint32_t parity, int *status) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((i & 255) == 0) {
+            if (load_volatile(status) != 0) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                record_status(status, QDQ_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // ---- bulk copy global -> shared (1-D, non-tensor, no multicast) -----------------
 // dst, src 16-byte aligned; bytes a multiple of 16. Completion is signalled as
 // transaction bytes on the mbarrier.

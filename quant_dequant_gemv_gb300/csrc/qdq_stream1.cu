@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
         bool prev_had = has_tiles(0);
         for (int L = 1; L < a.nlevels; ++L) {
             if (lane == 0) S1_TR(L, 0);
-            if (prev_had) mbar_wait(lvl_a, (lvl_phase++) & 1, status);
+            if (prev_had) mbar_wait_spin(lvl_a, (lvl_phase++) & 1, status);
             if (lane == 0) {
                 S1_TR(L, 1);
                 // The consumers' y stores are ordered before their arrivals (CTA
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
             if (had && lane == 0) mbar_arrive(dep_a);
             prev_had = had;
         }
-        if (prev_had) mbar_wait(lvl_a, (lvl_phase++) & 1, status);
+        if (prev_had) mbar_wait_spin(lvl_a, (lvl_phase++) & 1, status);
         if (lane == 0) {
             __threadfence();
             const unsigned old = atomicAdd(&a.counters[a.nlevels - 1], 1u);
@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 4);
             if (e != cur_e) {
                 if (dep_pending) {  // the previous level is complete on every CTA
-                    mbar_wait(dep_a, (dep_phase++) & 1, status);
+                    mbar_wait_spin(dep_a, (dep_phase++) & 1, status);
                     dep_pending = false;
                 }
                 cur_e = e;

@@ -286,6 +286,42 @@ def test_plan_run_io_host_buffers(q, orc):
     plan.close()
 
 
+def test_plan_chained_levels_read_previous_outputs(q, orc):
+    """A plan whose levels consume the previous level's outputs (x of level L+1 is a
+    y of level L), in every format and with side outputs, run twice. Each level is
+    checked against the oracle applied to the input it actually read from the GPU:
+    a level that started before its input was complete would have read NaN or
+    stale values (every y starts as NaN)."""
+    n = 2048
+    spec = [  # (level, name, format, rows, x from)
+        (0, "A", synth.Q4_K, n, "x0"), (0, "B", synth.Q6_K, 512, "x0"),
+        (1, "C", synth.Q6_K, n, "A"),
+        (2, "D", synth.Q8_0, n, "C"), (2, "E", synth.Q4_0, 1024, "C"),
+        (3, "F", synth.Q4_0, n, "D"),
+    ]
+    x0 = synth.gen_x(1, n, 4242)
+    bufs = {"x0": dev(x0)}
+    items, lv, Ws = [], [], {}
+    for li, name, t, rows, src in spec:
+        Ws[name] = synth.gen_matrix(t, rows, n, 300 + len(items))
+        bufs[name] = torch.full((1, rows), float("nan"), device="cuda")
+        items.append((t, dev(Ws[name]), rows, n, bufs[src], bufs[name]))
+        lv.append(li)
+    plan = q.Plan(items, lv, 1)
+    for _ in range(2):
+        for _, name, _, _, _ in spec:
+            bufs[name].fill_(float("nan"))
+        plan.run()
+        torch.cuda.synchronize()
+        assert q.get_device_status() == 0
+        got = {k: v.cpu().numpy() for k, v in bufs.items()}
+        for _, name, t, rows, src in spec:
+            assert not np.isnan(got[name]).any(), name
+            y_ref, S = orc.gemv(t, Ws[name], rows, n, got[src].astype(np.float32))
+            assert_close(got[name], y_ref, S, f"level output {name}")
+    plan.close()
+
+
 def test_full_decode_step_sampled(q, orc):
     """The 22-layer, 155-GEMV step in the launch configuration the benchmark
     times, checked on sampled rows of every GEMV."""
