@@ -185,6 +185,7 @@ def build_inputs(levels, batch, device, seed=0):
 
 L2_BYTES = 129 * 2 ** 20   # GB300 L2
 MMA_MIN_BATCH = 4          # single GEMVs from this batch on run on the tensor cores
+GROUP = 8                  # single-GEMV workloads: steps per replayed CUDA graph
 
 
 def gemv_launches(g, batch):
@@ -208,12 +209,16 @@ def run_ours(args, rank, world, device):
     if use_plan:
         items, lv, xs_host = build_inputs(levels, batch, device)
         plan = qdq.Plan(items, lv, batch)
-        step = lambda i: plan.run(stream)  # noqa: E731
         launches_per_step = plan.launches
+
+        def steps(i, n):
+            for _ in range(n):
+                plan.run(stream)
     else:
         # single GEMVs: rotate enough weight copies that W streams from HBM, not L2
         wbytes = sum(g.weight_bytes for lv_ in levels for g in lv_)
         ncopy = max(1, -(-4 * L2_BYTES // wbytes))
+        ncopy = -(-ncopy // GROUP) * GROUP  # whole groups of weight copies
         copies, xs_dev, ys, xs_host = [], [], [], []
         for li, level in enumerate(levels):
             x = synth.gen_x(batch, level[0].cols, 1000 + li)
@@ -230,27 +235,47 @@ def run_ours(args, rank, world, device):
                 for gi, g in enumerate(level):
                     qdq.gemv(g.qtype, cw[li][gi], g.rows, g.cols, xs_dev[li], ys[li][gi], batch, st)
         launches_per_step = sum(gemv_launches(g, batch) for lv_ in levels for g in lv_)
-        # the timed steps replay CUDA graphs of the same calls (one per weight copy),
-        # so the device time is not hidden behind the host cost of each call
+        # The timed steps replay CUDA graphs of the same calls: groups of GROUP
+        # consecutive steps (different weight copies) per graph, and single-step
+        # graphs for a remainder. Calls then run back to back on the device, as in
+        # a serving loop that captures its GEMVs, instead of each step waiting for
+        # its own graph launch.
         for i in range(3):
             step_api(i, stream)
         torch.cuda.synchronize(device)
-        graphs = []
+        single, grouped = [], []
         for c in range(ncopy):
             g_ = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_):
                 step_api(c, torch.cuda.current_stream(device))
-            graphs.append(g_)
+            single.append(g_)
+        for c0 in range(0, ncopy, GROUP):
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_):
+                for c in range(c0, c0 + GROUP):
+                    step_api(c, torch.cuda.current_stream(device))
+            grouped.append(g_)
         torch.cuda.synchronize(device)
-        step = lambda i: graphs[i % ncopy].replay()  # noqa: E731
+
+        def steps(i, n):
+            if n == GROUP:
+                grouped[(i % ncopy) // GROUP].replay()
+            else:
+                single[i % ncopy].replay()
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    for i in range(args.warmup):
-        step(i)
+    def group_len(i, left):  # steps run together from step i (a graph group when aligned)
+        return GROUP if (not use_plan and i % GROUP == 0 and left >= GROUP) else 1
+
+    i = 0
+    while i < args.warmup:
+        n = group_len(i, args.warmup - i)
+        steps(i, n)
+        i += n
     torch.cuda.synchronize(device)
     rc = qdq.get_device_status(stream)
     if rc != 0:
@@ -262,27 +287,32 @@ def run_ours(args, rank, world, device):
     i = 0
     while time.perf_counter() - t_load < 1.0:  # untimed load so the clock samples see a busy GPU
         for _ in range(50):
-            step(i)
+            steps(i, 1)
             i += 1
         torch.cuda.synchronize(device)
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    runs = []  # (steps, events) of each replay in the timed region
     barrier()
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        step(i)
-        ev[i][1].record(stream)
+    i = 0
+    while i < K:
+        n = group_len(i, K - i)
+        e = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        e[0].record(stream)
+        steps(i, n)
+        e[1].record(stream)
+        runs.append((n, e))
+        i += n
     t1.record(stream)
     torch.cuda.synchronize(device)
     barrier()
     clocks = sampler.stop()
     total_ms = t0.elapsed_time(t1)
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    launch_ms = [e[0].elapsed_time(e[1]) / n for n, e in runs for _ in range(n)]  # per step
     rc = qdq.get_device_status(stream)
     if rc != 0:
         raise SystemExit(f"device status after timing: {qdq.status_string(rc)}")
@@ -457,14 +487,17 @@ def main():
                        "step_bytes": abytes,
                        "l2": ("inputs larger than L2 (weights per step exceed 129 MB)" if args.workload == "step"
                               else "weights rotate over copies totalling at least 4x the 129 MB L2; "
-                                   "timed steps replay CUDA graphs of the qdq_gemv calls"),
+                                   f"timed steps replay CUDA graphs of the qdq_gemv calls, {GROUP} steps "
+                                   "(weight copies) per graph"),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic, "peak_source": peaks["source"],
-                         "kernel": ("stream_kernel (persistent plan launch)" if args.workload == "step"
+                         "kernel": ("stream1_kernel (persistent plan launch)" if args.workload == "step"
                                     else "mma_gemv_kernel + xsplit_kernel (tensor cores)"
-                                    if args.batch >= MMA_MIN_BATCH else "stream_kernel (one GEMV per launch)")},
+                                    if args.batch >= MMA_MIN_BATCH
+                                    else "stream1_kernel (one GEMV per launch)" if args.batch == 1
+                                    else "stream_kernel (one GEMV per launch)")},
             "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": r["launches"],
