@@ -184,13 +184,14 @@ def build_inputs(levels, batch, device, seed=0):
 
 
 L2_BYTES = 129 * 2 ** 20   # GB300 L2
-MMA_MIN_BATCH = 4          # single GEMVs from this batch on run on the tensor cores
+def mma_min_batch(qtype):  # single GEMVs from this batch on run on the tensor cores (library dispatch)
+    return 5 if qtype in (synth.Q4_K, synth.Q6_K) else 4
 GROUP = 8                  # single-GEMV workloads: steps per replayed CUDA graph
 
 
 def gemv_launches(g, batch):
     """Kernel launches of one qdq_gemv call (mirrors the library's dispatch)."""
-    if batch < MMA_MIN_BATCH:
+    if batch < mma_min_batch(g.qtype):
         return 1
     per = 32 if g.qtype == synth.Q6_K else 64
     return 2 * ((batch + per - 1) // per)  # split-x kernel + tensor-core kernel per batch slice
@@ -495,9 +496,8 @@ def main():
                          "traffic": traffic, "peak_source": peaks["source"],
                          "kernel": ("stream1_kernel (persistent plan launch)" if args.workload == "step"
                                     else "mma_gemv_kernel + xsplit_kernel (tensor cores)"
-                                    if args.batch >= MMA_MIN_BATCH
-                                    else "stream1_kernel (one GEMV per launch)" if args.batch == 1
-                                    else "stream_kernel (one GEMV per launch)")},
+                                    if args.batch >= mma_min_batch(levels[0][0].qtype)
+                                    else "stream1_kernel (one GEMV per launch)")},
             "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": r["launches"],

@@ -165,7 +165,7 @@ int qdq_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x
     cudaStream_t s = (cudaStream_t)stream;
     if (cols == 0)
         return cudaMemsetAsync(y, 0, (size_t)batch * rows * sizeof(float), s) == cudaSuccess ? QDQ_OK : QDQ_ERR_CUDA;
-    if (batch >= kMmaMinBatch) {
+    if (batch >= mma_min_batch(type)) {
         rc = launch_mma_gemv(type, W, rows, cols, x, y, batch, s, dev.sm_count);
         if (rc != QDQ_ERR_LIMIT) return rc;
         // shapes the tensor-core path does not take: batch slices of <= 8

@@ -31,7 +31,7 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
 
 int take_status_stream();
 // Batch-1 streaming kernel (qdq_stream1.cu): takes the same packed arguments.
-int stream1_launch(const void *args, bool big, bool cooperative, int grid, cudaStream_t stream);
+int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, cudaStream_t stream);
 int take_status_stream1();
 int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);
 
@@ -56,6 +56,10 @@ constexpr int kMaxPlanDescs = 192;
 constexpr int kMaxPlanLevels = 128;
 constexpr int kMaxGroupDescs = 8;
 constexpr int kStreamMaxBatch = 8;  // streaming kernel (plans, groups, small single GEMVs)
-constexpr int kMmaMinBatch = 4;     // single GEMVs from this batch on run on the tensor cores
+constexpr int kMmaMinBatch = 4;     // the tensor-core path takes batches from this one on
+// Single GEMVs run on the tensor cores from this batch on (measured crossover with
+// the CUDA-core streaming kernel on GB300: K-quants stream up to batch 4, the
+// 32-weight-block formats up to batch 3).
+inline int mma_min_batch(int type) { return (type == QDQ_Q4_K || type == QDQ_Q6_K) ? 5 : 4; }
 
 }  // namespace qdq

@@ -66,25 +66,36 @@ constexpr int kTileRows = 64;                     // rows of a whole-row tile (u
 constexpr int kChunkRows = 16;                    // rows of a chunked tile
 constexpr int kChunk = 2048;                      // columns of a chunk: kCW slices of kSlice
 constexpr int kSlice = 256;
-constexpr int kRingBytes = 172032;                // W ring: tiles packed in order, wrapping
-constexpr int kMaxTileBytes = kRingBytes / 2;     // at least two tiles in flight
 constexpr int kSlots = 8;                         // full/empty barrier pairs (tiles in the ring)
-constexpr int kXFloats = 1024;                    // private x area of one consumer warp
-constexpr int kBufRows = 512;                     // rows of the level partial buffer
 constexpr int kFlushBar = 1;                      // named barrier of the consumer warps
+constexpr int kPartFloats = 4096;                 // level partial buffer: [warp][row][batch column]
+
+// Per batch width BT (1, 2, 4, 8). Batch 1 keeps x in registers, staged per warp;
+// wider batches read x from one CTA-wide buffer holding every batch column.
+template <int BT>
+struct Cfg {
+    static constexpr int kRingBytes = BT == 1 ? 172032 : 114688;  // W ring: tiles packed in order
+    static constexpr int kMaxTileBytes = kRingBytes / 2;          // at least two tiles in flight
+    static constexpr int kXFloats = BT == 1 ? kCW * 1024 : 20480;  // x staging (per warp: 1024 at BT 1)
+    static constexpr int kBufRows = kPartFloats / (kCW * BT);      // rows of the level partial buffer
+    static constexpr int kNR = BT <= 4 ? 2 : 1;                    // rows per lane in one pass (BT > 1)
+};
 
 // Shared memory layout (bytes). The ring starts at 0 (1024-aligned base).
-template <int MAXD>
+template <int BT, int MAXD>
 struct Smem {
-    static constexpr int kX = kRingBytes;
-    static constexpr int kPart = kX + kCW * kXFloats * 4;     // [warp][buffer row] partials
-    static constexpr int kDst = kPart + kCW * kBufRows * 4;   // y address of each buffer row
-    static constexpr int kRanges = kDst + kBufRows * 8;
-    static constexpr int kRing = kRanges + 2 * MAXD * 8;      // producer: live tiles' ring ranges
+    static constexpr int kX = Cfg<BT>::kRingBytes;
+    static constexpr int kPart = kX + Cfg<BT>::kXFloats * 4;
+    static constexpr int kDst = kPart + kPartFloats * 4;               // y address of each buffer row
+    static constexpr int kDstStride = kDst + Cfg<BT>::kBufRows * 8;    // its batch-column stride (BT > 1)
+    static constexpr int kRanges = kDstStride + Cfg<BT>::kBufRows * 4;
+    static constexpr int kRing = kRanges + 2 * MAXD * 8;              // producer: live tiles' ring ranges
     static constexpr int kBars = kRing + 2 * kSlots * 4;
     static constexpr int kBytes = kBars + (2 * kSlots + 2) * 8;
 };
-static_assert(Smem<kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
+static_assert(Smem<1, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
+static_assert(Smem<2, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
+static_assert(Smem<8, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
 
 // ---------------------------------------------------------------------------
 // Tiles: identical sequence for the producer, the control warp and consumers.
@@ -104,29 +115,47 @@ struct Tile {
     bool first;       // first chunk of this row group in the window
     bool last;        // last chunk of this row group in the window
     bool first_win;   // the window starts at column 0 (y is stored, not accumulated)
+    int skinds;       // x copy kinds staged for this tile's epoch
 };
 
 QDQ_DEV int nkinds(int kinds) { return __popc(kinds & 7); }
-// x floats one warp stages per chunk: one 256-float slice per copy kind, plus the
-// eight Q4_K sub-block sums.
-QDQ_DEV int xfloats_per_chunk(int kinds) { return kSlice * nkinds(kinds) + ((kinds & 2) ? 8 : 0); }
+// x floats staged per chunk. Batch 1, per warp: one 256-float slice per copy kind
+// plus eight Q4_K sub-block sums. Wider batches, CTA-wide: the chunk's 2048 columns
+// of every batch column in every kind, plus eight sums per slice and column.
+template <int BT>
+QDQ_DEV int xfloats_per_chunk(int kinds) {
+    if constexpr (BT == 1) return kSlice * nkinds(kinds) + ((kinds & 2) ? 8 : 0);
+    else return (kChunk * nkinds(kinds) + kCW * 8) * BT;
+}
+template <int BT>
 QDQ_DEV int window_chunks(int kinds) {
-    const int w = kXFloats / xfloats_per_chunk(kinds);
+    const int cap = BT == 1 ? Cfg<1>::kXFloats / kCW : Cfg<BT>::kXFloats;
+    const int w = cap / xfloats_per_chunk<BT>(kinds);
     return w < 1 ? 1 : w;
+}
+// The kinds staged for a GEMV: every kind its level reads from this x when one
+// chunk of them fits, else only its own (the level's GEMVs then stage in turn).
+template <int BT>
+QDQ_DEV int staged_kinds(const DevDesc &d) {
+    const int cap = BT == 1 ? Cfg<1>::kXFloats / kCW : Cfg<BT>::kXFloats;
+    return xfloats_per_chunk<BT>(d.kinds) <= cap ? d.kinds : 1 << x_kind(d.type);
 }
 // Bytes of one row segment of a chunk, and the stage pitch of such segments.
 QDQ_DEV int seg_bytes(const DevDesc &d, int ccols) { return (ccols / blk_weights(d.type)) * blk_bytes(d.type); }
 QDQ_DEV int seg_pitch(int seg) { return ((seg + 15) & ~15) + 16; }
 // Rows of a whole-row tile (a multiple of 8 up to 64), or 0 when fewer than 8
 // rows fit a stage or the row's x does not fit one window.
-QDQ_DEV int whole_rows(const DevDesc &d) {
+template <int BT>
+QDQ_DEV int whole_rows(const DevDesc &d, int skinds) {
     const int nch = (d.cols + kChunk - 1) / kChunk;
-    const int cap = (kMaxTileBytes - 32) / d.rb;
-    if (cap < 8 || nch > window_chunks(d.kinds)) return 0;
-    return cap >= kTileRows ? kTileRows : cap & ~7;
+    const int cap = (Cfg<BT>::kMaxTileBytes - 32) / d.rb;
+    if (cap < 8 || nch > window_chunks<BT>(skinds)) return 0;
+    constexpr int rmax = kTileRows < Cfg<BT>::kBufRows ? kTileRows : Cfg<BT>::kBufRows;  // fits the partial buffer
+    return cap >= rmax ? rmax : cap & ~7;
 }
+template <int BT>
 QDQ_DEV int chunk_rows(const DevDesc &d) {
-    const int cap = kMaxTileBytes / seg_pitch(seg_bytes(d, kChunk));
+    const int cap = Cfg<BT>::kMaxTileBytes / seg_pitch(seg_bytes(d, kChunk));
     return cap < kChunkRows ? (cap < 1 ? 1 : cap) : kChunkRows;
 }
 
@@ -138,8 +167,9 @@ QDQ_DEV uint32_t tile_ring_bytes(const DevDesc &d, int nrows, bool whole, int cc
 }
 // Next tile's offset in the ring: packed after the previous one, or at 0 when it
 // would not fit before the end. Producer and consumers run the same sequence.
+template <int BT>
 QDQ_DEV uint32_t ring_place(uint32_t &next, uint32_t bytes) {
-    if (next + bytes > (uint32_t)kRingBytes) next = 0;
+    if (next + bytes > (uint32_t)Cfg<BT>::kRingBytes) next = 0;
     const uint32_t o = next;
     next += bytes;
     return o;
@@ -147,26 +177,28 @@ QDQ_DEV uint32_t ring_place(uint32_t &next, uint32_t bytes) {
 
 // on_begin(L) / on_end(L) around each level; on_tile(tile, epoch, desc) for every
 // tile. An epoch is one staged x window: (level, x, columns, window).
-template <class A, class FBegin, class FTile, class FEnd>
+template <int BT, class A, class FBegin, class FTile, class FEnd>
 QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&on_tile, FEnd &&on_end) {
     int epoch = -1;
     for (int L = 0; L < a.nlevels; ++L) {
         on_begin(L);
         const float *ex = nullptr;
-        int ew = -1, ecols = -1;
+        int ew = -1, ecols = -1, ekinds = -1;
         for (int g = a.level_start[L]; g < a.level_start[L + 1]; ++g) {
             const int64_t ra = ranges[2 * g], rb = ranges[2 * g + 1];
             if (ra >= rb) continue;
             const DevDesc d = a.d[g];
             const int nch = (d.cols + kChunk - 1) / kChunk;
             const int n = (int)(rb - ra);  // rows of one GEMV on one CTA
-            const int wr = whole_rows(d);
+            const int sk = staged_kinds<BT>(d);
+            const int wr = whole_rows<BT>(d, sk);
             if (wr > 0) {
-                if (d.x != ex || 0 != ew || d.cols != ecols) {
+                if (d.x != ex || 0 != ew || d.cols != ecols || sk != ekinds) {
                     ++epoch;
                     ex = d.x;
                     ew = 0;
                     ecols = d.cols;
+                    ekinds = sk;
                 }
                 for (int r = 0; r < n; r += wr) {
                     Tile t;
@@ -179,21 +211,23 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
                     t.xwn = nch;
                     t.whole = true;
                     t.first = t.last = t.first_win = true;
+                    t.skinds = sk;
                     on_tile(t, epoch, d);
                 }
                 continue;
             }
-            const int wmax = window_chunks(d.kinds);
-            const int nrmax = chunk_rows(d);
+            const int wmax = window_chunks<BT>(sk);
+            const int nrmax = chunk_rows<BT>(d);
             const int ntg = (n + nrmax - 1) / nrmax;
             const int nbase = n / ntg, nextra = n - nbase * ntg;
             for (int w0 = 0; w0 < nch; w0 += wmax) {
                 const int w1 = nch < w0 + wmax ? nch : w0 + wmax;
-                if (d.x != ex || w0 != ew || d.cols != ecols) {
+                if (d.x != ex || w0 != ew || d.cols != ecols || sk != ekinds) {
                     ++epoch;
                     ex = d.x;
                     ew = w0;
                     ecols = d.cols;
+                    ekinds = sk;
                 }
                 int64_t r = ra;
                 for (int tg = 0; tg < ntg; ++tg) {
@@ -211,6 +245,7 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
                         t.first = j == w0;
                         t.last = j == w1 - 1;
                         t.first_win = w0 == 0;
+                        t.skinds = sk;
                         on_tile(t, epoch, d);
                     }
                     r += nr;
@@ -282,10 +317,10 @@ QDQ_DEV int xunit(int u) { return (u & ~15) | ((u & 15) ^ ((u >> 3) & 6)); }
 
 // Stages x[col0 .. col0 + 2048 * (w1 - w0)) for warp w: slices of chunks w0..w1-1
 // in every copy kind, and the sub-block sums when Q4_K reads this x.
-QDQ_DEV void stage_x(const DevDesc &d, int w0, int w1, int w, int lane, float *area) {
-    const int kinds = d.kinds, nk = nkinds(kinds);
+QDQ_DEV void stage_x(const DevDesc &d, int kinds, int w0, int w1, int w, int lane, float *area) {
+    const int nk = nkinds(kinds);
     const int sums_off = (w1 - w0) * kSlice * nk;
-    constexpr int kMaxWin = kXFloats / kSlice;
+    constexpr int kMaxWin = Cfg<1>::kXFloats / kCW / kSlice;  // chunks of one kind in a warp area
     float4 v[2 * kMaxWin];
 #pragma unroll
     for (int j = 0; j < kMaxWin; ++j) {
@@ -359,22 +394,293 @@ QDQ_DEV void load_xr(const float *slice, int type, int c, XSlice &xr) {
     }
 }
 
-// Rows r (and r + 8 when NR == 2) x the lane's 64 columns of the warp's slice.
-// wrow[i] points at the slice in row i's segment; rows past the tile re-read the
-// tile's last row and their results are dropped.
-template <int NR>
-QDQ_DEV void slice_dot(int type, const uint8_t *const *wrow, int c, int nblk, const XSlice &xr, float (&out)[NR]) {
-    float acc[NR][1];
+// ---------------------------------------------------------------------------
+// Batch columns 2..8 (BT > 1). x for every batch column sits in one CTA-wide
+// buffer: per chunk of the window (stride xfloats_per_chunk<BT>), kind slot k,
+// column b and slice w at (k * BT + b) * 2048 + w * 256 (swizzled units), and the
+// eight Q4_K sub-block sums of (b, w) at nk * BT * 2048 + (b * 8 + w) * 8.
+// ---------------------------------------------------------------------------
+template <int BT>
+QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, int w, int lane, float *xbuf) {
+    const int nk = nkinds(kinds), stride = xfloats_per_chunk<BT>(kinds);
+    const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
+    for (int j = 0; w0 + j < w1; ++j) {
+        float *chunk = xbuf + j * stride;
+        const int col = (w0 + j) * kChunk + w * kSlice + 8 * lane;
 #pragma unroll
-    for (int r = 0; r < NR; ++r) acc[r][0] = 0.f;
-    if (type == QDQ_Q4_K) unit_q4k<1, NR>(wrow, c, xr, nullptr, 0, 0, nullptr, 0, acc);
-    else if (type == QDQ_Q6_K) unit_q6k<1, NR>(wrow, c, xr, nullptr, 0, 0, acc);
-    else if (2 * c < nblk) {
-        if (type == QDQ_Q8_0) unit_q8_0<1, NR>(wrow, c, nblk, xr, nullptr, 0, 0, acc);
-        else unit_q4_0<1, NR>(wrow, c, nblk, xr, nullptr, 0, 0, acc);
+        for (int b = 0; b < BT; ++b) {
+            const bool ok = b < batch && col < d.cols;
+            const float *xr = d.x + (int64_t)b * d.cols + col;
+            const float4 a = ok ? __ldcg((const float4 *)xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 c = ok ? __ldcg((const float4 *)(xr + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            int slot = 0;
+            if (kinds & 1) {
+                float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
+                sl[u0] = a;
+                sl[u1] = c;
+                ++slot;
+            }
+            if (kinds & 2) {  // Q4_K: columns 0..31 of each 64 meet low nibbles
+                const bool hi = (lane & 7) >= 4;
+                float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
+                sl[u0] = make_float4(a.x * nibble_scale(hi, 0), a.y * nibble_scale(hi, 1), a.z * nibble_scale(hi, 2),
+                                     a.w * nibble_scale(hi, 3));
+                sl[u1] = make_float4(c.x * nibble_scale(hi, 0), c.y * nibble_scale(hi, 1), c.z * nibble_scale(hi, 2),
+                                     c.w * nibble_scale(hi, 3));
+                ++slot;
+                float sm = ((a.x + a.y) + (a.z + a.w)) + ((c.x + c.y) + (c.z + c.w));
+                sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+                sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+                if ((lane & 3) == 0) chunk[nk * BT * kChunk + (b * 8 + w) * 8 + (lane >> 2)] = sm;
+            }
+            if (kinds & 4) {  // q4_0: columns 0..15 of each 32 meet low nibbles
+                const bool hi = (lane & 3) >= 2;
+                float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
+                sl[u0] = make_float4(a.x * nibble_scale(hi, 0), a.y * nibble_scale(hi, 1), a.z * nibble_scale(hi, 2),
+                                     a.w * nibble_scale(hi, 3));
+                sl[u1] = make_float4(c.x * nibble_scale(hi, 0), c.y * nibble_scale(hi, 1), c.z * nibble_scale(hi, 2),
+                                     c.w * nibble_scale(hi, 3));
+            }
+        }
+    }
+}
+
+// x pair units of column b: xs points at column 0's slice; columns are 2048 apart.
+QDQ_DEV void xpairs_b(const float *xs, int b, int u, uint64_t &p0, uint64_t &p1) {
+    const float4 v = ((const float4 *)(xs + b * kChunk))[xunit(u)];
+    p0 = bits2(__float_as_uint(v.x), __float_as_uint(v.y));
+    p1 = bits2(__float_as_uint(v.z), __float_as_uint(v.w));
+}
+
+// Q4_K, NR rows x BT columns: each word is decoded once and meets every column.
+template <int NR, int BT>
+QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const float *sums, float (&out)[NR][BT]) {
+    uint4 H[NR], Qa[NR], Qb[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        H[r] = ld4(wrow[r]);
+        Qa[r] = ld4(wrow[r] + 16 + 32 * c);
+        Qb[r] = ld4(wrow[r] + 32 + 32 * c);
+    }
+    const uint64_t M2 = bits2(__float_as_uint(kTwo23), __float_as_uint(kTwo23));
+    uint64_t lo[NR][BT], hi[NR][BT];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) lo[r][b] = hi[r][b] = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        uint64_t q0[NR], q1[NR], q2[NR], q3[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint32_t w[8] = {Qa[r].x, Qa[r].y, Qa[r].z, Qa[r].w, Qb[r].x, Qb[r].y, Qb[r].z, Qb[r].w};
+            const uint32_t v = w[t], u = v >> 16;
+            q0[r] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2);
+            q1[r] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2);
+            q2[r] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2);
+            q3[r] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2);
+        }
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            uint64_t xl0, xl1, xh0, xh1;
+            xpairs_b(xs, b, 16 * c + t, xl0, xl1);
+            xpairs_b(xs, b, 16 * c + 8 + t, xh0, xh1);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                lo[r][b] = ffma2(q1[r], xl1, ffma2(q0[r], xl0, lo[r][b]));
+                hi[r][b] = ffma2(q3[r], xh1, ffma2(q2[r], xh0, hi[r][b]));
+            }
+        }
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) out[r] = acc[r][0];
+    for (int r = 0; r < NR; ++r) {
+        uint32_t sc2, mn2;
+        q4k_pair_fields(H[r].y, H[r].z, H[r].w, c, &sc2, &mn2);
+        const float d = half_bits_to_float(H[r].x & 0xFFFF), dmin = half_bits_to_float(H[r].x >> 16);
+        const float sl = (float)(sc2 & 0xFF), sh = (float)(sc2 >> 8), ml = (float)(mn2 & 0xFF), mh = (float)(mn2 >> 8);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const float l = lo_of(lo[r][b]) + hi_of(lo[r][b]), h = lo_of(hi[r][b]) + hi_of(hi[r][b]);
+            out[r][b] = d * (sl * l + sh * h) - dmin * (ml * sums[b * 64 + 2 * c] + mh * sums[b * 64 + 2 * c + 1]);
+        }
+    }
+}
+
+// Q6_K, c = 2 h + m (see dot_q6k), NR rows x BT columns.
+template <int NR, int BT>
+QDQ_DEV void dotb_q6k(const uint8_t *const *wrow, int c, const float *xs, float (&out)[NR][BT]) {
+    const int h = c >> 1, m = c & 1;
+    uint32_t ql0[NR][4], ql1[NR][4], qh[NR][4], scw[NR][2], dw[NR][1];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const uint8_t *sb = wrow[r];  // 2-byte aligned
+        ld_words_a2<4>(sb + 64 * h + 16 * m, ql0[r]);
+        ld_words_a2<4>(sb + 64 * h + 32 + 16 * m, ql1[r]);
+        ld_words_a2<4>(sb + 128 + 32 * h + 16 * m, qh[r]);
+        ld_words_a2<2>(sb + 192 + 8 * h, scw[r]);
+        ld_words_a2<1>(sb + 208, dw[r]);
+    }
+    const uint64_t M32 = bits2(__float_as_uint(kTwo23 + 32.0f), __float_as_uint(kTwo23 + 32.0f));
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) out[r][b] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint64_t acc[NR][BT];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[r][b] = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            uint64_t p0[NR], p1[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const uint32_t b6 = q6k_quant_bytes((k & 1) ? ql1[r][t] : ql0[r][t], qh[r][t], k);
+                p0[r] = fsub2(bits2(byte_to_magic<0>(b6), byte_to_magic<1>(b6)), M32);
+                p1[r] = fsub2(bits2(byte_to_magic<2>(b6), byte_to_magic<3>(b6)), M32);
+            }
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                uint64_t x0, x1;
+                xpairs_b(xs, b, 32 * h + 8 * k + 4 * m + t, x0, x1);
+#pragma unroll
+                for (int r = 0; r < NR; ++r) acc[r][b] = ffma2(p1[r], x1, ffma2(p0[r], x0, acc[r][b]));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const int byte = m + 2 * k;
+            const uint32_t word = byte < 4 ? scw[r][0] : scw[r][1];
+            const float sc = (float)(int)(int8_t)((word >> (8 * (byte & 3))) & 0xFF);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) out[r][b] += sc * (lo_of(acc[r][b]) + hi_of(acc[r][b]));
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const float d = half_bits_to_float(dw[r][0] & 0xFFFF);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) out[r][b] *= d;
+    }
+}
+
+// q8_0, NR rows x BT columns; nb = blocks of the slice inside the row.
+template <int NR, int BT>
+QDQ_DEV void dotb_q8_0(const uint8_t *const *wrow, int c, int nb, const float *xs, float (&out)[NR][BT]) {
+    const uint64_t M128 = bits2(__float_as_uint(kTwo23 + 128.0f), __float_as_uint(kTwo23 + 128.0f));
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) out[r][b] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        if (2 * c + i >= nb) break;
+        uint32_t q[NR][9];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint32_t *base = (const uint32_t *)(wrow[r] + 72 * c + 36 * i);
+#pragma unroll
+            for (int t = 0; t < 9; ++t) q[r][t] = base[t];
+        }
+        uint64_t acc[NR][BT];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[r][b] = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            uint64_t p0[NR], p1[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const uint32_t v = q[r][1 + t] ^ 0x80808080u;
+                p0[r] = fsub2(bits2(byte_to_magic<0>(v), byte_to_magic<1>(v)), M128);
+                p1[r] = fsub2(bits2(byte_to_magic<2>(v), byte_to_magic<3>(v)), M128);
+            }
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                uint64_t x0, x1;
+                xpairs_b(xs, b, 16 * c + 8 * i + t, x0, x1);
+#pragma unroll
+                for (int r = 0; r < NR; ++r) acc[r][b] = ffma2(p1[r], x1, ffma2(p0[r], x0, acc[r][b]));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+                out[r][b] += __uint_as_float(q[r][0]) * (lo_of(acc[r][b]) + hi_of(acc[r][b]));
+    }
+}
+
+// q4_0, NR rows x BT columns (see dot_q4_0 for the nibble layout).
+template <int NR, int BT>
+QDQ_DEV void dotb_q4_0(const uint8_t *const *wrow, int c, int nb, const float *xs, float (&out)[NR][BT]) {
+    const uint64_t C_la = bits2(__float_as_uint(kTwo23 + 8.0f), __float_as_uint(kTwo23 + 2048.0f));
+    const uint64_t C_lb = bits2(__float_as_uint(kTwo23 + 524288.0f), __float_as_uint(kTwo23 + 2048.0f));
+    const uint64_t C_h = bits2(__float_as_uint(kTwo23 + 128.0f), __float_as_uint(kTwo23 + 32768.0f));
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) out[r][b] = 0.f;
+    if (2 * c >= nb) return;  // the slice ends before this lane's blocks
+    const bool v1 = 2 * c + 1 < nb;
+    uint32_t qs[NR][8];
+    float d[NR][2];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        uint32_t w[9];
+        if (v1) {
+            ld_words_a2<9>(wrow[r] + 36 * c, w);
+        } else {
+            uint32_t w5[5];
+            ld_words_a2<5>(wrow[r] + 36 * c, w5);
+#pragma unroll
+            for (int i = 0; i < 5; ++i) w[i] = w5[i];
+#pragma unroll
+            for (int i = 5; i < 9; ++i) w[i] = 0x88888888u;
+        }
+        d[r][0] = half_bits_to_float(w[0] & 0xFFFF);
+        d[r][1] = v1 ? half_bits_to_float(w[4] >> 16) : 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) qs[r][t] = __funnelshift_r(w[t], w[t + 1], 16);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) qs[r][4 + t] = w[5 + t];
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        uint64_t acc[NR][BT];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) acc[r][b] = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            uint64_t p0[NR], p1[NR], p2[NR], p3[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const uint32_t v = qs[r][4 * i + t], u = v >> 16;
+                p0[r] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), C_la);
+                p1[r] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), C_lb);
+                p2[r] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), C_h);
+                p3[r] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), C_h);
+            }
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                uint64_t xl0, xl1, xh0, xh1;
+                xpairs_b(xs, b, 16 * c + 8 * i + t, xl0, xl1);
+                xpairs_b(xs, b, 16 * c + 8 * i + 4 + t, xh0, xh1);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    acc[r][b] = ffma2(p3[r], xh1, ffma2(p2[r], xh0, ffma2(p1[r], xl1, ffma2(p0[r], xl0, acc[r][b]))));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) out[r][b] += d[r][i] * (lo_of(acc[r][b]) + hi_of(acc[r][b]));
+    }
 }
 
 // Shared-memory addresses of a tile's rows: whole rows are contiguous (one
@@ -401,8 +707,8 @@ QDQ_DEV void tile_slices(const Tile &tl, const DevDesc &d, const uint8_t *stage_
     constexpr int QK = (TYPE == QDQ_Q4_K || TYPE == QDQ_Q6_K) ? 256 : 32;
     constexpr int SB = (kSlice / QK) * blk_bytes(TYPE);  // slice bytes
     constexpr int KIND = x_kind(TYPE);
-    const int nk = nkinds(d.kinds);
-    const int slot = __popc(d.kinds & ((1 << KIND) - 1));
+    const int nk = nkinds(tl.skinds);
+    const int slot = __popc(tl.skinds & ((1 << KIND) - 1));
     const int nslices = (tl.ccols + kSlice - 1) / kSlice;
     const int k0 = tl.whole ? cw : 8 * tl.chunk + cw;
     const int kend = tl.whole ? nslices : (cw < nslices ? k0 + 1 : k0);
@@ -426,26 +732,26 @@ QDQ_DEV void tile_slices(const Tile &tl, const DevDesc &d, const uint8_t *stage_
             if (left > 8) {
                 const int rb = r8 + 8 < left ? rp + r8 + 8 : tl.nrows - 1;
                 const uint8_t *wrow[2] = {row_ptr(stage_p, geo, rp + r8) + koff, row_ptr(stage_p, geo, rb) + koff};
-                float acc[2][1] = {{0.f}, {0.f}};
-                if constexpr (TYPE == QDQ_Q4_K) unit_q4k<1, 2>(wrow, c, xr, nullptr, 0, 0, nullptr, 0, acc);
-                else if constexpr (TYPE == QDQ_Q6_K) unit_q6k<1, 2>(wrow, c, xr, nullptr, 0, 0, acc);
+                float acc[2] = {0.f, 0.f};
+                if constexpr (TYPE == QDQ_Q4_K) unit_q4k<2>(wrow, c, xr, acc);
+                else if constexpr (TYPE == QDQ_Q6_K) unit_q6k<2>(wrow, c, xr, acc);
                 else if (2 * c < nb) {
-                    if constexpr (TYPE == QDQ_Q8_0) unit_q8_0<1, 2>(wrow, c, nb, xr, nullptr, 0, 0, acc);
-                    else unit_q4_0<1, 2>(wrow, c, nb, xr, nullptr, 0, 0, acc);
+                    if constexpr (TYPE == QDQ_Q8_0) unit_q8_0<2>(wrow, c, nb, xr, acc);
+                    else unit_q4_0<2>(wrow, c, nb, xr, acc);
                 }
-                o0 = acc[0][0];
-                o1 = acc[1][0];
+                o0 = acc[0];
+                o1 = acc[1];
             } else {
                 const int ra = r8 < left ? rp + r8 : tl.nrows - 1;
                 const uint8_t *wrow[1] = {row_ptr(stage_p, geo, ra) + koff};
-                float acc[1][1] = {{0.f}};
-                if constexpr (TYPE == QDQ_Q4_K) unit_q4k<1, 1>(wrow, c, xr, nullptr, 0, 0, nullptr, 0, acc);
-                else if constexpr (TYPE == QDQ_Q6_K) unit_q6k<1, 1>(wrow, c, xr, nullptr, 0, 0, acc);
+                float acc[1] = {0.f};
+                if constexpr (TYPE == QDQ_Q4_K) unit_q4k<1>(wrow, c, xr, acc);
+                else if constexpr (TYPE == QDQ_Q6_K) unit_q6k<1>(wrow, c, xr, acc);
                 else if (2 * c < nb) {
-                    if constexpr (TYPE == QDQ_Q8_0) unit_q8_0<1, 1>(wrow, c, nb, xr, nullptr, 0, 0, acc);
-                    else unit_q4_0<1, 1>(wrow, c, nb, xr, nullptr, 0, 0, acc);
+                    if constexpr (TYPE == QDQ_Q8_0) unit_q8_0<1>(wrow, c, nb, xr, acc);
+                    else unit_q4_0<1>(wrow, c, nb, xr, acc);
                 }
-                o0 = acc[0][0];
+                o0 = acc[0];
             }
             o0 += __shfl_xor_sync(0xffffffffu, o0, 1);
             o1 += __shfl_xor_sync(0xffffffffu, o1, 1);
@@ -463,16 +769,91 @@ QDQ_DEV void tile_slices(const Tile &tl, const DevDesc &d, const uint8_t *stage_
         for (int rr = r8; rr < tl.nrows; rr += 8) mycol[rr] = 0.f;
 }
 
+// Batch columns 2..8: rows r, r + 8, ... (NR; lane 4 r + c) of one slice against
+// every column; the row partials go to this warp's column of the level buffer as
+// [row][batch column].
+template <int TYPE, int NR, int BT>
+QDQ_DEV void pass_rows_b(const uint8_t *stage_p, const RowGeo &geo, uint32_t koff, int rp, int left, int r8, int c,
+                         int nb, const float *xs, const float *sums, bool fresh, float *mycol) {
+    const uint8_t *wrow[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int r = r8 + 8 * i;
+        wrow[i] = row_ptr(stage_p, geo, rp + (r < left ? r : left - 1)) + koff;
+    }
+    float acc[NR][BT];
+    if constexpr (TYPE == QDQ_Q4_K) dotb_q4k<NR, BT>(wrow, c, xs, sums, acc);
+    else if constexpr (TYPE == QDQ_Q6_K) dotb_q6k<NR, BT>(wrow, c, xs, acc);
+    else if constexpr (TYPE == QDQ_Q8_0) dotb_q8_0<NR, BT>(wrow, c, nb, xs, acc);
+    else dotb_q4_0<NR, BT>(wrow, c, nb, xs, acc);
+#pragma unroll
+    for (int i = 0; i < NR; ++i)
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            acc[i][b] += __shfl_xor_sync(0xffffffffu, acc[i][b], 1);
+            acc[i][b] += __shfl_xor_sync(0xffffffffu, acc[i][b], 2);
+        }
+    if (c == 0) {
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+            const int r = r8 + 8 * i;
+            if (r < left) {
+                float *q = mycol + (rp + r) * BT;
+#pragma unroll
+                for (int b = 0; b < BT; ++b) q[b] = fresh ? acc[i][b] : q[b] + acc[i][b];
+            }
+        }
+    }
+}
+
+template <int TYPE, int BT>
+QDQ_DEV void tile_slices_b(const Tile &tl, const DevDesc &d, const uint8_t *stage_p, const RowGeo &geo,
+                           const float *xbuf, int cw, int r8, int c, float *mycol) {
+    constexpr int QK = (TYPE == QDQ_Q4_K || TYPE == QDQ_Q6_K) ? 256 : 32;
+    constexpr int SB = (kSlice / QK) * blk_bytes(TYPE);
+    constexpr int KIND = x_kind(TYPE);
+    constexpr int NR = Cfg<BT>::kNR;
+    const int nk = nkinds(tl.skinds);
+    const int slot = __popc(tl.skinds & ((1 << KIND) - 1));
+    const int stride = xfloats_per_chunk<BT>(tl.skinds);
+    const int nslices = (tl.ccols + kSlice - 1) / kSlice;
+    const int k0 = tl.whole ? cw : 8 * tl.chunk + cw;
+    const int kend = tl.whole ? nslices : (cw < nslices ? k0 + 1 : k0);
+    const int n = tl.nrows;
+    bool fresh = tl.first;
+    for (int k = k0; k < kend; k += kCW) {
+        const float *chunk = xbuf + ((k >> 3) - tl.xw0) * stride;
+        const float *xs = chunk + slot * BT * kChunk + (k & 7) * kSlice;
+        const float *sums = chunk + nk * BT * kChunk + (k & 7) * 8;
+        const int kcols = d.cols - k * kSlice;
+        const int nb = (kcols < kSlice ? kcols : kSlice) / QK;
+        const uint32_t koff = (uint32_t)(tl.whole ? k : cw) * SB;
+        for (int rp = 0; rp < n; rp += 8 * NR) {
+            if (NR == 2 && n - rp > 8)
+                pass_rows_b<TYPE, NR, BT>(stage_p, geo, koff, rp, n - rp, r8, c, nb, xs, sums, fresh, mycol);
+            else
+                pass_rows_b<TYPE, 1, BT>(stage_p, geo, koff, rp, n - rp, r8, c, nb, xs, sums, fresh, mycol);
+        }
+        fresh = false;
+    }
+    if (fresh && c == 0)  // no slice of this warp in the tile: zero partials
+        for (int rr = r8; rr < n; rr += 8)
+#pragma unroll
+            for (int b = 0; b < BT; ++b) mycol[rr * BT + b] = 0.f;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int MAXD, int MAXL>
+template <int BT, int MAXD, int MAXL>
 __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_constant__ StreamArgs<MAXD, MAXL> a) {
-    using SM = Smem<MAXD>;
+    using SM = Smem<BT, MAXD>;
+    constexpr int kBufRows = Cfg<BT>::kBufRows;
     extern __shared__ __align__(1024) uint8_t smem[];
-    float *xareas = (float *)(smem + SM::kX);
+    float *xareas = (float *)(smem + SM::kX);  // batch 1: per-warp x areas; wider: one CTA-wide buffer
     float *part = (float *)(smem + SM::kPart);
     uint64_t *dst = (uint64_t *)(smem + SM::kDst);
+    int *dstride = (int *)(smem + SM::kDstStride);
     int64_t *ranges = (int64_t *)(smem + SM::kRanges);
     const uint32_t ring_a = smem_u32(smem);
     const uint32_t full_a = smem_u32(smem + SM::kBars), empty_a = full_a + 8 * kSlots;
@@ -508,11 +889,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
         int t = 0, rel = 0;
         uint32_t next = 0;
         uint32_t *toff = (uint32_t *)(smem + SM::kRing), *tlen = toff + kSlots;
-        walk(
+        walk<BT>(
             a, ranges, [](int) {},
             [&](const Tile &tl, int, const DevDesc &d) {
                 const uint32_t bytes = tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols);
-                const uint32_t o = ring_place(next, bytes);
+                const uint32_t o = ring_place<BT>(next, bytes);
                 for (;;) {
                     bool block = rel < t && rel <= t - kSlots;
                     for (int j = rel; !block && j < t; ++j) {
@@ -584,19 +965,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
     const int cw = warp - kFirstCW;
     const int ctid = (int)threadIdx.x - 32 * kFirstCW;
     const int r8 = lane >> 2, c = lane & 3;
-    float *area = xareas + cw * kXFloats;
-    float *mypart = part + cw * kBufRows;
+    float *area = BT == 1 ? xareas + cw * (Cfg<1>::kXFloats / kCW) : xareas;
+    float *mypart = part + cw * kBufRows * BT;
     int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0, dep_phase = 0;
     int buf_rows = 0, rg_base = 0;
     uint32_t ring_next = 0;
-    bool had_tiles = false, dep_pending = false;
+    bool had_tiles = false, dep_pending = false, level_staged = false;
     (void)cur_level;
 
     // Adds the eight warps' partials of every buffered row (warp order) and stores
     // y (adding to it for rows whose earlier columns were stored before).
     auto flush = [&]() {
         named_bar_sync(kFlushBar, kCW * 32);  // partials and addresses are in place
-        for (int i = ctid; i < buf_rows; i += kCW * 32) {
+        for (int i = ctid; BT == 1 && i < buf_rows; i += kCW * 32) {
             float sum = 0.f;
 #pragma unroll
             for (int w = 0; w < kCW; ++w) sum += part[w * kBufRows + i];
@@ -605,16 +986,29 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
             if (d & 1) sum += __ldcg(yp);
             *yp = sum;
         }
+        // batch columns: entry i of a warp's column is (row i / BT, column i % BT)
+        for (int i = ctid; BT > 1 && i < buf_rows * BT; i += kCW * 32) {
+            const int row = i / BT, b = i - row * BT;
+            if (b >= a.batch) continue;
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) sum += part[w * kBufRows * BT + i];
+            const uint64_t d = dst[row];
+            float *yp = (float *)(uintptr_t)(d & ~(uint64_t)1) + (int64_t)b * dstride[row];
+            if (d & 1) sum += __ldcg(yp);
+            *yp = sum;
+        }
         named_bar_sync(kFlushBar, kCW * 32);  // the buffer may be refilled
         buf_rows = 0;
     };
 
-    walk(
+    walk<BT>(
         a, ranges,
         [&](int L) {
             cur_level = L;
             tiles_in_level = 0;
             dep_pending = L > 0 && levels_synced;
+            level_staged = false;
         },
         [&](const Tile &tl, int e, const DevDesc &d) {
             had_tiles = true;
@@ -625,7 +1019,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                     dep_pending = false;
                 }
                 cur_e = e;
-                stage_x(d, tl.xw0, tl.xw0 + tl.xwn, cw, lane, area);
+                if constexpr (BT == 1) {
+                    stage_x(d, tl.skinds, tl.xw0, tl.xw0 + tl.xwn, cw, lane, area);
+                } else {
+                    // the buffer is shared: a later x of the same level waits for every
+                    // warp to be done with it; then every warp stages its slices
+                    if (level_staged) named_bar_sync(kFlushBar, kCW * 32);
+                    stage_xb<BT>(d, tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, lane, area);
+                    named_bar_sync(kFlushBar, kCW * 32);
+                    level_staged = true;
+                }
             }
             if (tl.first) {  // a new row group: its rows in the partial buffer
                 // Rows whose earlier columns sit in this buffer are stored first.
@@ -634,11 +1037,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                 buf_rows += tl.nrows;
                 if (cw == 0)
                     for (int i = lane; i < tl.nrows; i += 32)
-                        dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) | (tl.first_win ? 0u : 1u);
+                        dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) | (tl.first_win ? 0u : 1u),
+                        dstride[rg_base + i] = (int)d.rows;
             }
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 5);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 8 + 3 * tiles_in_level);
-            const uint32_t toffs = ring_place(ring_next, tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols));
+            const uint32_t toffs = ring_place<BT>(ring_next, tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols));
             const int s = t % kSlots;
             mbar_wait(full_a + 8 * s, (t / kSlots) & 1, status);
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 6);
@@ -656,12 +1060,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                     geo.src_lo = (uint32_t)(uintptr_t)(d.W + tl.row0 * d.rb + chunk_off(d, tl.chunk));
                     geo.pitch = seg_pitch(seg_bytes(d, tl.ccols));
                 }
-                float *mycol = mypart + rg_base;
-                switch (d.type) {
-                    case QDQ_Q4_K: tile_slices<QDQ_Q4_K>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                    case QDQ_Q6_K: tile_slices<QDQ_Q6_K>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                    case QDQ_Q8_0: tile_slices<QDQ_Q8_0>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                    default: tile_slices<QDQ_Q4_0>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                float *mycol = mypart + rg_base * BT;
+                if constexpr (BT == 1) {
+                    switch (d.type) {
+                        case QDQ_Q4_K: tile_slices<QDQ_Q4_K>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        case QDQ_Q6_K: tile_slices<QDQ_Q6_K>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        case QDQ_Q8_0: tile_slices<QDQ_Q8_0>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        default: tile_slices<QDQ_Q4_0>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                    }
+                } else {
+                    switch (d.type) {
+                        case QDQ_Q4_K: tile_slices_b<QDQ_Q4_K, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        case QDQ_Q6_K: tile_slices_b<QDQ_Q6_K, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        case QDQ_Q8_0: tile_slices_b<QDQ_Q8_0, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        default: tile_slices_b<QDQ_Q4_0, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                    }
                 }
             }
             __syncwarp();
@@ -686,10 +1099,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int MAXD, int MAXL>
+template <int BT, int MAXD, int MAXL>
 static int launch1(const void *args, int grid, bool cooperative, cudaStream_t stream) {
-    auto kern = s1::stream1_kernel<MAXD, MAXL>;
-    constexpr int smem = s1::Smem<MAXD>::kBytes;
+    auto kern = s1::stream1_kernel<BT, MAXD, MAXL>;
+    constexpr int smem = s1::Smem<BT, MAXD>::kBytes;
     RelaxedCaptureScope relaxed;  // the first launch sets the kernel's attributes
     static bool attr_done[64] = {};
     int dev = 0;
@@ -714,9 +1127,20 @@ static int launch1(const void *args, int grid, bool cooperative, cudaStream_t st
     return QDQ_OK;
 }
 
-int stream1_launch(const void *args, bool big, bool cooperative, int grid, cudaStream_t stream) {
-    return big ? launch1<kMaxPlanDescs, kMaxPlanLevels>(args, grid, cooperative, stream)
-               : launch1<kMaxGroupDescs, 1>(args, grid, cooperative, stream);
+template <int BT>
+static int launch1_bt(const void *args, bool big, bool cooperative, int grid, cudaStream_t stream) {
+    return big ? launch1<BT, kMaxPlanDescs, kMaxPlanLevels>(args, grid, cooperative, stream)
+               : launch1<BT, kMaxGroupDescs, 1>(args, grid, cooperative, stream);
+}
+
+int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, cudaStream_t stream) {
+    switch (bt) {
+        case 1: return launch1_bt<1>(args, big, cooperative, grid, stream);
+        case 2: return launch1_bt<2>(args, big, cooperative, grid, stream);
+        case 4: return launch1_bt<4>(args, big, cooperative, grid, stream);
+        case 8: return launch1_bt<8>(args, big, cooperative, grid, stream);
+        default: return QDQ_ERR_LIMIT;
+    }
 }
 
 int take_status_stream1() {

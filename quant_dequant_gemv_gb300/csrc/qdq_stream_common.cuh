@@ -1,6 +1,6 @@
-// qdq_stream_common.cuh -- pieces shared by the two streaming (CUDA-core) GEMV
-// kernels: the packed kernel arguments, the format constants, the per-CTA row
-// split, the bulk-copy helper and the per-format dequant-dot units.
+// qdq_stream_common.cuh -- pieces of the streaming (CUDA-core) GEMV kernel that
+// the host-side plan packing shares with it: the packed kernel arguments, the
+// format constants, the bulk-copy helper and the batch-1 dequant-dot units.
 //
 // "S21 The Capstone: picoLM, in Python", section 3 (fused dequant + dot product:
 // the quantised bytes are decoded in registers and multiplied straight into the
@@ -20,9 +20,9 @@ struct DevDesc {
     int32_t cols;
     int32_t type;
     int32_t rb;     // bytes per row
-    int32_t kc;     // columns per x chunk
+    int32_t pad0;   // keeps the fields below at the offsets the kernel's register allocation was tuned with
     int32_t kinds;  // bit k: the level's x needs swizzled copy kind k (0 plain, 1 Q4_K-scaled, 2 q4_0-scaled)
-    int32_t pad;
+    int32_t pad1;
 };
 
 template <int MAXD, int MAXL>
@@ -43,49 +43,6 @@ __host__ __device__ constexpr int blk_bytes(int t) {
 __host__ __device__ constexpr int blk_weights(int t) { return (t == QDQ_Q4_K || t == QDQ_Q6_K) ? 256 : 32; }
 __host__ __device__ constexpr int x_kind(int t) { return t == QDQ_Q4_K ? 1 : t == QDQ_Q4_0 ? 2 : 0; }
 
-// Float offsets inside an x slot: the swizzled copies in kind order, each
-// [batch][kc] floats.
-QDQ_DEV int copy_offset(int kinds, int kind, int kc, int BT) {
-    int off = 0;
-    for (int k = 0; k < kind; ++k)
-        if ((kinds >> k) & 1) off += kc * BT;
-    return off;
-}
-
-// Swizzled x layout: the 16-byte chunk c of a staged row is stored at chunk
-// c ^ rev3((c >> 4) & 7). Lanes read 64-float runs at 256-byte strides (Q4_K,
-// q8_0, q4_0) or 16-float runs at 64/512/1024-byte offsets (Q6_K); with the
-// swizzle the eight lanes of each quarter-warp hit eight different bank groups.
-QDQ_DEV int xswz(int c) {
-    const int v = (c >> 4) & 7;
-    return c ^ (((v & 1) << 2) | (v & 2) | (v >> 2));
-}
-// Four floats at logical offset `off` (a multiple of 4) of a swizzled row.
-QDQ_DEV uint4 xload4(const float *row, int off) { return *(const uint4 *)(row + 4 * xswz(off >> 2)); }
-
-template <class A>
-QDQ_DEV void cta_rows(const A &a, int L, int g, int cta, int P, int64_t *ra, int64_t *rb) {
-    int64_t total = 0, start = 0;
-    for (int i = a.level_start[L]; i < a.level_start[L + 1]; ++i) {
-        const int64_t bytes = a.d[i].rows * (int64_t)a.d[i].rb;
-        if (i < g) start += bytes;
-        total += bytes;
-    }
-    const int64_t A0 = (int64_t)cta * total / P, B0 = (int64_t)(cta + 1) * total / P;
-    const int64_t rbytes = a.d[g].rb, rows = a.d[g].rows;
-    auto row_at = [&](int64_t byte) -> int64_t {
-        const int64_t off = byte - start;
-        if (off <= 0) return 0;
-        const int64_t r = (off + rbytes - 1) / rbytes;
-        return r < rows ? r : rows;
-    };
-    *ra = row_at(A0);
-    *rb = row_at(B0);
-}
-
-// Calls on_begin(L) / on_end(L) around each level and on_tile(tile, geom, epoch,
-// new_epoch, desc) for every tile. An epoch is one staged x: (level, x buffer,
-// chunk).
 // ---------------------------------------------------------------------------
 // Producer: bulk copies of a tile's bytes into a stage.
 // Copies [floor16(src), min(ceil16(end), floor16(W_end))) in bulk and any last
@@ -115,13 +72,12 @@ QDQ_DEV uint32_t copy_span(const uint8_t *src, uint32_t len, const uint8_t *w_en
 }
 
 // ---------------------------------------------------------------------------
-// Consumer: per-format work on NR rows x one column block.
-//   wrow[r]: first byte of this column block in row r (shared memory).
-//   xr:      batch 1: the lane's 64 x values as 32 float pairs (pre-scaled for
-//            the nibble formats) and, for Q4_K, the sums of x over its two
-//            sub-blocks; shared by the NR rows.
-//   xs:      batch > 1 (NR = 1): the lane's x slice for batch 0 in the matching
-//            staged copy; batch b is at xs + b * xstride floats.
+// Consumer: per-format work on NR rows x the lane's 64 columns, batch 1.
+//   wrow[r]: first byte of the unit's super-block (Q4_K, Q6_K) or block pair
+//            (q8_0, q4_0) in row r, in shared memory.
+//   xr:      the lane's 64 x values as 32 float pairs (pre-scaled for the nibble
+//            formats) and, for Q4_K, the sums of x over its two sub-blocks;
+//            shared by the NR rows.
 // Shared memory is read with plain loads through pointers into the dynamic
 // shared array, so the compiler can interleave the rows' loads and arithmetic.
 // ---------------------------------------------------------------------------
@@ -146,45 +102,11 @@ QDQ_DEV void ld_words_a2(const uint8_t *p, uint32_t (&out)[N]) {
     for (int i = 0; i < N; ++i) out[i] = __funnelshift_r(w[i], w[i + 1], sh);
 }
 
-QDQ_DEV void load_pairs16(const float *row, int off, uint64_t *dst) {  // 16 floats -> 8 pairs
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint4 v = xload4(row, off + 4 * i);
-        dst[2 * i] = bits2(v.x, v.y);
-        dst[2 * i + 1] = bits2(v.z, v.w);
-    }
-}
-
-template <int TYPE>
-QDQ_DEV int lane_col0(int lane) {
-    if constexpr (TYPE == QDQ_Q4_K) return 256 * (lane >> 2) + 64 * (lane & 3);
-    else if constexpr (TYPE == QDQ_Q6_K) return 256 * (lane >> 2) + 128 * ((lane >> 1) & 1) + 16 * (lane & 1);
-    else return 64 * lane;
-}
-
-template <int TYPE>
-QDQ_DEV void load_x(const float *xrow, int off, const float *xsum, XSlice &x) {
-    if constexpr (TYPE == QDQ_Q6_K) {  // four runs of 16 at stride 32
-#pragma unroll
-        for (int k = 0; k < 4; ++k) load_pairs16(xrow, off + 32 * k, &x.v[8 * k]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) load_pairs16(xrow, off + 16 * k, &x.v[8 * k]);
-    }
-    if constexpr (TYPE == QDQ_Q4_K) {
-        x.s0 = xsum[0];
-        x.s1 = xsum[1];
-    }
-}
-
-QDQ_DEV uint64_t pairsum_zero() { return 0; }
-
 // Q4_K: lane = 4 s + c covers chunk c of super-block s: sub-block 2c (low nibbles,
 // x[0..31] of the slice) and 2c+1 (high nibbles, x[32..63]).
 // sum = d * (sc_lo * sum(q x)_lo + sc_hi * sum(q x)_hi) - dmin * (mn_lo * sum(x)_lo + mn_hi * sum(x)_hi)
-template <int BT, int NR>
-QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, const float *xrow, int xoff,
-                      int xstride, const float *xsum, int xsum_stride, float (&out)[NR][BT]) {
+template <int NR>
+QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, float (&out)[NR]) {
     const int s = lane >> 2, c = lane & 3;
     uint4 H[NR], Qa[NR], Qb[NR];
 #pragma unroll
@@ -203,56 +125,26 @@ QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, co
         const float sc_lo = (float)(sc2 & 0xFF), sc_hi = (float)(sc2 >> 8);
         const float mn_lo = (float)(mn2 & 0xFF), mn_hi = (float)(mn2 >> 8);
         const uint32_t w[8] = {Qa[r].x, Qa[r].y, Qa[r].z, Qa[r].w, Qb[r].x, Qb[r].y, Qb[r].z, Qb[r].w};
-        if constexpr (BT == 1) {
-            uint64_t a0 = 0, a1 = 0, h0 = 0, h1 = 0;
+        uint64_t a0 = 0, a1 = 0, h0 = 0, h1 = 0;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t v = w[t], u = v >> 16;
-                a0 = ffma2(fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2), xr.v[2 * t], a0);
-                a1 = ffma2(fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2), xr.v[2 * t + 1], a1);
-                h0 = ffma2(fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2), xr.v[16 + 2 * t], h0);
-                h1 = ffma2(fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2), xr.v[17 + 2 * t], h1);
-            }
-            const float lo = (lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1));
-            const float hi = (lo_of(h0) + hi_of(h0)) + (lo_of(h1) + hi_of(h1));
-            out[r][0] = d * (sc_lo * lo + sc_hi * hi) - dmin * (mn_lo * xr.s0 + mn_hi * xr.s1);
-        } else {
-            uint64_t q[32];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t v = w[t], u = v >> 16;
-                q[2 * t] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2);
-                q[2 * t + 1] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2);
-                q[16 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2);
-                q[17 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2);
-            }
-#pragma unroll
-            for (int b = 0; b < BT; ++b) {
-                const float *xb = xrow + b * xstride;
-                uint64_t a0 = 0, a1 = 0, h0 = 0, h1 = 0;
-#pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const uint4 xl = xload4(xb, xoff + 2 * i), xh = xload4(xb, xoff + 32 + 2 * i);
-                    a0 = ffma2(q[i], bits2(xl.x, xl.y), a0);
-                    a1 = ffma2(q[i + 1], bits2(xl.z, xl.w), a1);
-                    h0 = ffma2(q[16 + i], bits2(xh.x, xh.y), h0);
-                    h1 = ffma2(q[17 + i], bits2(xh.z, xh.w), h1);
-                }
-                const float lo = (lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1));
-                const float hi = (lo_of(h0) + hi_of(h0)) + (lo_of(h1) + hi_of(h1));
-                const float s0 = xsum[b * xsum_stride], s1 = xsum[b * xsum_stride + 1];
-                out[r][b] = d * (sc_lo * lo + sc_hi * hi) - dmin * (mn_lo * s0 + mn_hi * s1);
-            }
+        for (int t = 0; t < 8; ++t) {
+            const uint32_t v = w[t], u = v >> 16;
+            a0 = ffma2(fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2), xr.v[2 * t], a0);
+            a1 = ffma2(fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2), xr.v[2 * t + 1], a1);
+            h0 = ffma2(fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2), xr.v[16 + 2 * t], h0);
+            h1 = ffma2(fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2), xr.v[17 + 2 * t], h1);
         }
+        const float lo = (lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1));
+        const float hi = (lo_of(h0) + hi_of(h0)) + (lo_of(h1) + hi_of(h1));
+        out[r] = d * (sc_lo * lo + sc_hi * hi) - dmin * (mn_lo * xr.s0 + mn_hi * xr.s1);
     }
 }
 
 // Q6_K: lane = 4 s + 2 h + m covers, in super-block s, half h and the 16-wide
 // column group m of each of the four 32-runs k: elements 128h + 32k + 16m + l,
 // l < 16, with scale scales[8h + 2k + m] (= element / 16).
-template <int BT, int NR>
-QDQ_DEV void unit_q6k(const uint8_t *const *wrow, int lane, const XSlice &xr, const float *xrow, int xoff,
-                      int xstride, float (&out)[NR][BT]) {
+template <int NR>
+QDQ_DEV void unit_q6k(const uint8_t *const *wrow, int lane, const XSlice &xr, float (&out)[NR]) {
     const int s = lane >> 2, h = (lane >> 1) & 1, m = lane & 1;
     uint32_t ql0[NR][4], ql1[NR][4], qh[NR][4], scw[NR][2], dw[NR][1];
 #pragma unroll
@@ -275,60 +167,27 @@ QDQ_DEV void unit_q6k(const uint8_t *const *wrow, int lane, const XSlice &xr, co
             const uint32_t word = byte < 4 ? scw[r][0] : scw[r][1];
             sc[k] = (float)(int)(int8_t)((word >> (8 * (byte & 3))) & 0xFF);
         }
-        if constexpr (BT == 1) {
-            float sum = 0.f;
+        float sum = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint64_t a0 = 0, a1 = 0;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t b6 = q6k_quant_bytes((k & 1) ? ql1[r][t] : ql0[r][t], qh[r][t], k);
-                    a0 = ffma2(fsub2(bits2(byte_to_magic<0>(b6), byte_to_magic<1>(b6)), M32), xr.v[8 * k + 2 * t], a0);
-                    a1 = ffma2(fsub2(bits2(byte_to_magic<2>(b6), byte_to_magic<3>(b6)), M32), xr.v[8 * k + 2 * t + 1],
-                               a1);
-                }
-                sum += sc[k] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
-            }
-            out[r][0] = d * sum;
-        } else {
-            uint64_t q[32];
+        for (int k = 0; k < 4; ++k) {
+            uint64_t a0 = 0, a1 = 0;
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t b6 = q6k_quant_bytes((k & 1) ? ql1[r][t] : ql0[r][t], qh[r][t], k);
-                    q[8 * k + 2 * t] = fsub2(bits2(byte_to_magic<0>(b6), byte_to_magic<1>(b6)), M32);
-                    q[8 * k + 2 * t + 1] = fsub2(bits2(byte_to_magic<2>(b6), byte_to_magic<3>(b6)), M32);
-                }
+                const uint32_t b6 = q6k_quant_bytes((k & 1) ? ql1[r][t] : ql0[r][t], qh[r][t], k);
+                a0 = ffma2(fsub2(bits2(byte_to_magic<0>(b6), byte_to_magic<1>(b6)), M32), xr.v[8 * k + 2 * t], a0);
+                a1 = ffma2(fsub2(bits2(byte_to_magic<2>(b6), byte_to_magic<3>(b6)), M32), xr.v[8 * k + 2 * t + 1], a1);
             }
-#pragma unroll
-            for (int b = 0; b < BT; ++b) {
-                float sum = 0.f;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float *xb = xrow + b * xstride;
-                    uint64_t a0 = 0, a1 = 0;
-#pragma unroll
-                    for (int i = 0; i < 8; i += 2) {
-                        const uint4 xv = xload4(xb, xoff + 32 * k + 2 * i);
-                        a0 = ffma2(q[8 * k + i], bits2(xv.x, xv.y), a0);
-                        a1 = ffma2(q[8 * k + i + 1], bits2(xv.z, xv.w), a1);
-                    }
-                    sum += sc[k] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
-                }
-                out[r][b] = d * sum;
-            }
+            sum += sc[k] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
         }
+        out[r] = d * sum;
     }
 }
 
-// q8_0: lane covers blocks 2*lane and 2*lane+1 of the column block (x[0..31],
-// x[32..63] of the slice). An int8 q becomes 2^23 + (q + 128) by flipping its
-// sign bit and placing the byte under the exponent; subtracting 2^23 + 128
-// leaves q exactly.
-template <int BT, int NR>
-QDQ_DEV void unit_q8_0(const uint8_t *const *wrow, int lane, int nblk_valid, const XSlice &xr, const float *xrow,
-                       int xoff, int xstride, float (&out)[NR][BT]) {
+// q8_0: lane covers blocks 2*lane and 2*lane+1 of the slice (x[0..31], x[32..63]
+// of its 64). An int8 q becomes 2^23 + (q + 128) by flipping its sign bit and
+// placing the byte under the exponent; subtracting 2^23 + 128 leaves q exactly.
+template <int NR>
+QDQ_DEV void unit_q8_0(const uint8_t *const *wrow, int lane, int nblk_valid, const XSlice &xr, float (&out)[NR]) {
     const uint64_t M128 = bits2(__float_as_uint(kTwo23 + 128.0f), __float_as_uint(kTwo23 + 128.0f));
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -346,31 +205,18 @@ QDQ_DEV void unit_q8_0(const uint8_t *const *wrow, int lane, int nblk_valid, con
                 q[16 * i + 2 * t + 1] = fsub2(bits2(byte_to_magic<2>(v), byte_to_magic<3>(v)), M128);
             }
         }
+        float sum = 0.f;
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-            float sum = 0.f;
+        for (int i = 0; i < 2; ++i) {
+            uint64_t a0 = 0, a1 = 0;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                uint64_t a0 = 0, a1 = 0;
-                if constexpr (BT == 1) {
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        a0 = ffma2(q[16 * i + j], xr.v[16 * i + j], a0);
-                        a1 = ffma2(q[16 * i + j + 1], xr.v[16 * i + j + 1], a1);
-                    }
-                } else {
-                    const float *xb = xrow + b * xstride;
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const uint4 xv = xload4(xb, xoff + 32 * i + 2 * j);
-                        a0 = ffma2(q[16 * i + j], bits2(xv.x, xv.y), a0);
-                        a1 = ffma2(q[16 * i + j + 1], bits2(xv.z, xv.w), a1);
-                    }
-                }
-                sum += d[i] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
+            for (int j = 0; j < 16; j += 2) {
+                a0 = ffma2(q[16 * i + j], xr.v[16 * i + j], a0);
+                a1 = ffma2(q[16 * i + j + 1], xr.v[16 * i + j + 1], a1);
             }
-            out[r][b] = sum;
+            sum += d[i] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
         }
+        out[r] = sum;
     }
 }
 
@@ -378,9 +224,8 @@ QDQ_DEV void unit_q8_0(const uint8_t *const *wrow, int lane, int nblk_valid, con
 // of a block holds weight i (low nibble) and weight i+16 (high nibble). Nibbles
 // stay at their bit position p (x pre-scaled by 2^-p); subtracting 2^23 + 8*2^p
 // gives (q - 8) * 2^p exactly.
-template <int BT, int NR>
-QDQ_DEV void unit_q4_0(const uint8_t *const *wrow, int lane, int nblk_valid, const XSlice &xr, const float *xrow,
-                       int xoff, int xstride, float (&out)[NR][BT]) {
+template <int NR>
+QDQ_DEV void unit_q4_0(const uint8_t *const *wrow, int lane, int nblk_valid, const XSlice &xr, float (&out)[NR]) {
     const uint64_t C_la = bits2(__float_as_uint(kTwo23 + 8.0f), __float_as_uint(kTwo23 + 2048.0f));
     const uint64_t C_lb = bits2(__float_as_uint(kTwo23 + 524288.0f), __float_as_uint(kTwo23 + 2048.0f));
     const uint64_t C_h = bits2(__float_as_uint(kTwo23 + 128.0f), __float_as_uint(kTwo23 + 32768.0f));
@@ -418,50 +263,19 @@ QDQ_DEV void unit_q4_0(const uint8_t *const *wrow, int lane, int nblk_valid, con
                 q[16 * i + 9 + 2 * t] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), C_h);
             }
         }
+        float sum = 0.f;
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-            float sum = 0.f;
+        for (int i = 0; i < 2; ++i) {
+            uint64_t a0 = 0, a1 = 0;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                uint64_t a0 = 0, a1 = 0;
-                if constexpr (BT == 1) {
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        a0 = ffma2(q[16 * i + j], xr.v[16 * i + j], a0);
-                        a1 = ffma2(q[16 * i + j + 1], xr.v[16 * i + j + 1], a1);
-                    }
-                } else {
-                    const float *xb = xrow + b * xstride;
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const uint4 xv = xload4(xb, xoff + 32 * i + 2 * j);
-                        a0 = ffma2(q[16 * i + j], bits2(xv.x, xv.y), a0);
-                        a1 = ffma2(q[16 * i + j + 1], bits2(xv.z, xv.w), a1);
-                    }
-                }
-                sum += d[i] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
+            for (int j = 0; j < 16; j += 2) {
+                a0 = ffma2(q[16 * i + j], xr.v[16 * i + j], a0);
+                a1 = ffma2(q[16 * i + j + 1], xr.v[16 * i + j + 1], a1);
             }
-            out[r][b] = sum;
+            sum += d[i] * ((lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1)));
         }
+        out[r] = sum;
     }
-}
-
-QDQ_DEV float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// Sums of a over lanes and of b over lanes in one tree: afterwards lane 0 holds
-// sum(a) and lane 16 holds sum(b).
-QDQ_DEV float warp_sum2(float a, float b, int lane) {
-    const bool upper = lane & 16;
-    float keep = upper ? b : a;
-    const float send = upper ? a : b;
-    keep += __shfl_xor_sync(0xffffffffu, send, 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-    return keep;
 }
 
 // Scale that puts x next to a nibble read at its bit position (see unit_q4k /
@@ -471,30 +285,6 @@ QDQ_DEV float nibble_scale(bool high, int p) {
     const float lo = p == 0 ? 1.f : p == 2 ? 1.52587890625e-05f : 0.00390625f;
     const float hi = (p & 1) ? 0.000244140625f : 0.0625f;
     return high ? hi : lo;
-}
-
-// NR rows x one column block for the desc's format, into out (zero where the
-// lane has nothing in this block).
-template <int BT, int NR>
-QDQ_DEV void run_unit(int type, const uint8_t *const *wrow, int lane, int cols_here, const XSlice &xr,
-                      const float *xrow, int xoff, int xstride, const float *xsum, int xsum_stride,
-                      float (&out)[NR][BT]) {
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-#pragma unroll
-        for (int b = 0; b < BT; ++b) out[r][b] = 0.f;
-    if (type == QDQ_Q4_K) {
-        if (256 * (lane >> 2) < cols_here)
-            unit_q4k<BT, NR>(wrow, lane, xr, xrow, xoff, xstride, xsum, xsum_stride, out);
-    } else if (type == QDQ_Q6_K) {
-        if (256 * (lane >> 2) < cols_here) unit_q6k<BT, NR>(wrow, lane, xr, xrow, xoff, xstride, out);
-    } else {
-        const int nblk = cols_here / 32;
-        if (2 * lane < nblk) {
-            if (type == QDQ_Q8_0) unit_q8_0<BT, NR>(wrow, lane, nblk, xr, xrow, xoff, xstride, out);
-            else unit_q4_0<BT, NR>(wrow, lane, nblk, xr, xrow, xoff, xstride, out);
-        }
-    }
 }
 
 }  // namespace qdq

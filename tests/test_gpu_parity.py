@@ -286,12 +286,13 @@ def test_plan_run_io_host_buffers(q, orc):
     plan.close()
 
 
-def test_plan_chained_levels_read_previous_outputs(q, orc):
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_plan_chained_levels_read_previous_outputs(q, orc, batch):
     """A plan whose levels consume the previous level's outputs (x of level L+1 is a
-    y of level L), in every format and with side outputs, run twice. Each level is
-    checked against the oracle applied to the input it actually read from the GPU:
-    a level that started before its input was complete would have read NaN or
-    stale values (every y starts as NaN)."""
+    y of level L), in every format and with side outputs, run twice, at batch 1, 3
+    (a padded batch width) and 8. Each level is checked against the oracle applied
+    to the input it actually read from the GPU: a level that started before its
+    input was complete would have read NaN or stale values (every y starts as NaN)."""
     n = 2048
     spec = [  # (level, name, format, rows, x from)
         (0, "A", synth.Q4_K, n, "x0"), (0, "B", synth.Q6_K, 512, "x0"),
@@ -299,15 +300,15 @@ def test_plan_chained_levels_read_previous_outputs(q, orc):
         (2, "D", synth.Q8_0, n, "C"), (2, "E", synth.Q4_0, 1024, "C"),
         (3, "F", synth.Q4_0, n, "D"),
     ]
-    x0 = synth.gen_x(1, n, 4242)
+    x0 = synth.gen_x(batch, n, 4242)
     bufs = {"x0": dev(x0)}
     items, lv, Ws = [], [], {}
     for li, name, t, rows, src in spec:
         Ws[name] = synth.gen_matrix(t, rows, n, 300 + len(items))
-        bufs[name] = torch.full((1, rows), float("nan"), device="cuda")
+        bufs[name] = torch.full((batch, rows), float("nan"), device="cuda")
         items.append((t, dev(Ws[name]), rows, n, bufs[src], bufs[name]))
         lv.append(li)
-    plan = q.Plan(items, lv, 1)
+    plan = q.Plan(items, lv, batch)
     for _ in range(2):
         for _, name, _, _, _ in spec:
             bufs[name].fill_(float("nan"))
@@ -318,6 +319,7 @@ def test_plan_chained_levels_read_previous_outputs(q, orc):
         for _, name, t, rows, src in spec:
             assert not np.isnan(got[name]).any(), name
             y_ref, S = orc.gemv(t, Ws[name], rows, n, got[src].astype(np.float32))
+            assert y_ref.shape == (batch, rows)
             assert_close(got[name], y_ref, S, f"level output {name}")
     plan.close()
 
