@@ -63,7 +63,7 @@ constexpr int kFirstCW = 2;                       // warp 0 producer, warp 1 con
 constexpr int kThreads = 32 * (kCW + kFirstCW);
 constexpr int kPassRows = 16;                     // rows of one pass (lanes cover r and r + 8)
 constexpr int kTileRows = 64;                     // rows of a whole-row tile (up to four passes)
-constexpr int kChunkRows = 16;                    // rows of a chunked tile
+constexpr int kChunkRows = 32;                    // rows of a chunked tile
 constexpr int kChunk = 2048;                      // columns of a chunk: kCW slices of kSlice
 constexpr int kSlice = 256;
 constexpr int kSlots = 8;                         // full/empty barrier pairs (tiles in the ring)
@@ -99,13 +99,16 @@ static_assert(Smem<8, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budge
 
 // ---------------------------------------------------------------------------
 // Tiles: identical sequence for the producer, the control warp and consumers.
-// A whole-row tile holds up to 64 complete rows (one contiguous bulk copy) and
-// every chunk of their x; rows too long for 8 per stage are cut into 2048-column
-// chunks of up to 16 rows, copied row segment by row segment.
+// A whole-row tile holds up to 64 complete rows and every chunk of their x. It
+// is one contiguous bulk copy, except for rows whose length is a multiple of 128
+// bytes read with 32-bit loads: those are copied row by row to a pitch 16 bytes
+// longer, so that the eight rows a warp reads at once fall in different shared-
+// memory banks. Rows too long for 8 per stage are cut into 2048-column chunks of
+// up to 32 rows, copied row segment by row segment at a padded pitch.
 // ---------------------------------------------------------------------------
 struct Tile {
     int g;            // GEMV (desc index)
-    int nrows;        // 1..64 (whole rows) or 1..16 (chunked)
+    int nrows;        // 1..64 (whole rows) or 1..32 (chunked)
     int64_t row0;
     int chunk;        // chunked: the 2048-column chunk; whole rows: 0
     int ccols;        // columns of the tile (whole rows: all of them)
@@ -143,12 +146,19 @@ QDQ_DEV int staged_kinds(const DevDesc &d) {
 // Bytes of one row segment of a chunk, and the stage pitch of such segments.
 QDQ_DEV int seg_bytes(const DevDesc &d, int ccols) { return (ccols / blk_weights(d.type)) * blk_bytes(d.type); }
 QDQ_DEV int seg_pitch(int seg) { return ((seg + 15) & ~15) + 16; }
+// Whole rows copied one by one to a padded pitch (see the tile comment above):
+// the formats read with 32-bit loads (Q6_K, q8_0, q4_0), rows of at least 2 KiB
+// whose length is a multiple of 128 bytes, and a 16-byte aligned matrix.
+QDQ_DEV bool rows_padded(const DevDesc &d) {
+    return d.type != QDQ_Q4_K && d.rb >= 2048 && (d.rb & 127) == 0 && ((uintptr_t)d.W & 15) == 0;
+}
+QDQ_DEV int whole_pitch(const DevDesc &d) { return rows_padded(d) ? d.rb + 16 : d.rb; }
 // Rows of a whole-row tile (a multiple of 8 up to 64), or 0 when fewer than 8
 // rows fit a stage or the row's x does not fit one window.
 template <int BT>
 QDQ_DEV int whole_rows(const DevDesc &d, int skinds) {
     const int nch = (d.cols + kChunk - 1) / kChunk;
-    const int cap = (Cfg<BT>::kMaxTileBytes - 32) / d.rb;
+    const int cap = (Cfg<BT>::kMaxTileBytes - 32) / whole_pitch(d);
     if (cap < 8 || nch > window_chunks<BT>(skinds)) return 0;
     constexpr int rmax = kTileRows < Cfg<BT>::kBufRows ? kTileRows : Cfg<BT>::kBufRows;  // fits the partial buffer
     return cap >= rmax ? rmax : cap & ~7;
@@ -160,9 +170,10 @@ QDQ_DEV int chunk_rows(const DevDesc &d) {
 }
 
 // Bytes a tile takes in the ring (copy_span may start up to 15 bytes before and
-// end up to 15 bytes after the tile's rows; chunk segments sit at their pitch).
+// end up to 15 bytes after the tile's rows; padded rows and chunk segments sit at
+// their pitch).
 QDQ_DEV uint32_t tile_ring_bytes(const DevDesc &d, int nrows, bool whole, int ccols) {
-    const uint32_t b = whole ? (uint32_t)(nrows * d.rb + 32) : (uint32_t)(nrows * seg_pitch(seg_bytes(d, ccols)));
+    const uint32_t b = whole ? (uint32_t)(nrows * whole_pitch(d) + 32) : (uint32_t)(nrows * seg_pitch(seg_bytes(d, ccols)));
     return (b + 127u) & ~127u;
 }
 // Next tile's offset in the ring: packed after the previous one, or at 0 when it
@@ -285,22 +296,34 @@ QDQ_DEV void cta_rows_by_gemv(const A &a, int L, int g, int cta, int P, int64_t 
     *rb = (l + 1) * rows / n;
 }
 
-// Byte offset of chunk j inside a row, and the shared-memory address of row
-// `row`'s segment of the tile in a stage (it keeps the source's offset mod 16).
+// Byte offset of chunk j inside a row.
 QDQ_DEV int64_t chunk_off(const DevDesc &d, int j) {
     return (int64_t)j * (kChunk / blk_weights(d.type)) * blk_bytes(d.type);
 }
-QDQ_DEV uint32_t seg_addr(const DevDesc &d, const Tile &t, uint32_t stage, int r) {
-    if (t.whole) return stage + (uint32_t)((uintptr_t)(d.W + t.row0 * d.rb) & 15) + (uint32_t)r * d.rb;
-    const uint8_t *src = d.W + (t.row0 + r) * d.rb + chunk_off(d, t.chunk);
-    return stage + (uint32_t)r * seg_pitch(seg_bytes(d, t.ccols)) + (uint32_t)((uintptr_t)src & 15);
+// n copies of len bytes, src advancing by sstride and dst by dstride: every
+// address and length a multiple of 16, so nothing is over-read.
+QDQ_DEV void copy_rows(const uint8_t *src, int64_t sstride, uint32_t dst, uint32_t dstride, uint32_t len, int n,
+                       uint32_t bar) {
+    const uint64_t pol = policy_evict_first();
+    for (int r = 0; r < n; ++r, src += sstride, dst += dstride) bulk_g2s_hint(dst, src, len, bar, pol);
 }
-// Producer side: bulk copies of the tile into a stage (see copy_span).
+// Producer side: bulk copies of the tile into a stage. Returns the bulk byte
+// count; mode kTail stores the trailing bytes of an unaligned matrix end, kBulk
+// issues the copies (see copy_span).
 QDQ_DEV uint32_t tile_copy(const DevDesc &d, const Tile &t, uint32_t stage, uint32_t bar, int mode) {
     const uint8_t *w_end = d.W + d.rows * (int64_t)d.rb;
-    if (t.whole) return copy_span(d.W + t.row0 * d.rb, (uint32_t)t.nrows * d.rb, w_end, stage, bar, mode);
+    if (t.whole) {
+        if (!rows_padded(d)) return copy_span(d.W + t.row0 * d.rb, (uint32_t)t.nrows * d.rb, w_end, stage, bar, mode);
+        if (mode & kBulk) copy_rows(d.W + t.row0 * d.rb, d.rb, stage, (uint32_t)whole_pitch(d), (uint32_t)d.rb, t.nrows, bar);
+        return (uint32_t)(t.nrows * d.rb);
+    }
     const int seg = seg_bytes(d, t.ccols), pitch = seg_pitch(seg);
     const int64_t off = chunk_off(d, t.chunk);
+    const uint8_t *src = d.W + t.row0 * d.rb + off;
+    if ((((uintptr_t)src | (uintptr_t)d.rb | (uintptr_t)seg) & 15) == 0) {  // every segment aligned
+        if (mode & kBulk) copy_rows(src, d.rb, stage, (uint32_t)pitch, (uint32_t)seg, t.nrows, bar);
+        return (uint32_t)(t.nrows * seg);
+    }
     uint32_t total = 0;
     for (int r = 0; r < t.nrows; ++r)
         total += copy_span(d.W + (t.row0 + r) * d.rb + off, (uint32_t)seg, w_end, stage + (uint32_t)(r * pitch), bar,
@@ -684,12 +707,12 @@ QDQ_DEV void dotb_q4_0(const uint8_t *const *wrow, int c, int nb, const float *x
 }
 
 // Shared-memory addresses of a tile's rows: whole rows are contiguous (one
-// copy that keeps the source's offset mod 16); chunk segments sit at a fixed
-// pitch, each keeping its own source offset mod 16.
+// copy that keeps the source's offset mod 16); padded rows and chunk segments
+// sit at a fixed pitch, each keeping its own source offset mod 16.
 struct RowGeo {
     uint32_t src_lo;  // low bits of the global address of row 0's first tile byte
     int rb;           // row bytes in global memory
-    int pitch;        // stage pitch of chunk segments (0: whole rows)
+    int pitch;        // stage pitch of padded rows or chunk segments (0: contiguous rows)
 };
 QDQ_DEV const uint8_t *row_ptr(const uint8_t *stage_p, const RowGeo &g, int r) {
     if (g.pitch == 0) return stage_p + (g.src_lo & 15u) + (uint32_t)(r * g.rb);
@@ -1055,7 +1078,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                 geo.rb = d.rb;
                 if (tl.whole) {
                     geo.src_lo = (uint32_t)(uintptr_t)(d.W + tl.row0 * d.rb);
-                    geo.pitch = 0;
+                    geo.pitch = rows_padded(d) ? whole_pitch(d) : 0;
                 } else {
                     geo.src_lo = (uint32_t)(uintptr_t)(d.W + tl.row0 * d.rb + chunk_off(d, tl.chunk));
                     geo.pitch = seg_pitch(seg_bytes(d, tl.ccols));

@@ -136,6 +136,20 @@ def test_gemv_wide_rows_column_chunks(q, orc, qtype, cols):
         assert_close(y, y_ref, S, f"{synth.TYPE_NAMES[qtype]} cols {cols} batch {batch}")
 
 
+@pytest.mark.parametrize("qtype,rows,cols", [(synth.Q8_0, 3648, 16384), (synth.Q4_0, 3000, 4096),
+                                             (synth.Q8_0, 3000, 4096), (synth.Q4_0, 2000, 32800),
+                                             (synth.Q6_K, 2000, 16896)])
+def test_gemv_many_rows_per_cta(q, orc, qtype, rows, cols):
+    # 13-24 rows per CTA: multi-pass tiles of padded whole rows (row length a
+    # multiple of 128 bytes) and of column chunks (aligned and unaligned rows)
+    for batch in (1, 3):
+        W = synth.gen_matrix(qtype, rows, cols, 75)
+        x = synth.gen_x(batch, cols, 76)
+        y = run_gemv(q, qtype, W, rows, cols, x)
+        y_ref, S = orc.gemv(qtype, W, rows, cols, x)
+        assert_close(y, y_ref, S, f"{synth.TYPE_NAMES[qtype]} {rows}x{cols} batch {batch}")
+
+
 def test_gemv_guard_bytes_and_determinism(q, orc):
     qtype, rows, cols = synth.Q6_K, 77, 5632
     W = synth.gen_matrix(qtype, rows, cols, 80)
