@@ -58,8 +58,9 @@ constexpr int kMaxGroupDescs = 8;
 constexpr int kStreamMaxBatch = 8;  // streaming kernel (plans, groups, small single GEMVs)
 constexpr int kMmaMinBatch = 4;     // the tensor-core path takes batches from this one on
 // Single GEMVs run on the tensor cores from this batch on (measured crossover with
-// the CUDA-core streaming kernel on GB300: K-quants stream up to batch 4, the
-// 32-weight-block formats up to batch 3).
-inline int mma_min_batch(int type) { return (type == QDQ_Q4_K || type == QDQ_Q6_K) ? 5 : 4; }
+// the CUDA-core streaming kernel on GB300: every format streams faster up to
+// batch 4, which its four-column instantiation covers; from batch 5 the streaming
+// kernel runs its eight-column instantiation and the tensor cores win).
+inline int mma_min_batch(int /*type*/) { return 5; }
 
 }  // namespace qdq
