@@ -37,7 +37,10 @@ static __device__ int s_status_s1;
 
 // Phase timestamps for performance analysis, compiled in only with -DQDQ_TRACE:
 // trace[(cta * nlevels + level) * 32 + slot] = %globaltimer (S1_TR) or the SM's
-// clock64 (S1_TRC, per-tile phases of the first consumer warp).
+// clock64 (S1_TRC, per-tile phases of the first consumer warp). Slots: 0-2 control
+// warp, 4-7 consumer level phases, 8-28 per tile (before the full wait, after it,
+// after processing), 29 producer reaches the level's first tile, 30-31 producer
+// has issued the level's first and second tile.
 #ifdef QDQ_TRACE
 #define S1_TR(L, slot)                                                                                  \
     do {                                                                                                \
@@ -912,9 +915,15 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
         int t = 0, rel = 0;
         uint32_t next = 0;
         uint32_t *toff = (uint32_t *)(smem + SM::kRing), *tlen = toff + kSlots;
+        int plevel = 0, ptile = 0;  // trace builds: level and tile within it
         walk<BT>(
-            a, ranges, [](int) {},
+            a, ranges,
+            [&](int L) {
+                plevel = L;
+                ptile = 0;
+            },
             [&](const Tile &tl, int, const DevDesc &d) {
+                if (ptile == 0) S1_TR(plevel, 29);
                 const uint32_t bytes = tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols);
                 const uint32_t o = ring_place<BT>(next, bytes);
                 for (;;) {
@@ -934,9 +943,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                 const uint32_t nb = tile_copy(d, tl, stage, bar, kTail);
                 mbar_arrive_expect_tx(bar, nb);  // releases the tail stores above
                 tile_copy(d, tl, stage, bar, kBulk);
+                if (ptile < 2) S1_TR(plevel, 30 + ptile);
+                ++ptile;
                 ++t;
             },
             [](int) {});
+        (void)plevel;
         for (int i = t - kSlots > 0 ? t - kSlots : 0; i < t; ++i)  // no exit with copies in flight
             mbar_wait(full_a + 8 * (i % kSlots), (i / kSlots) & 1, status);
         return;
