@@ -83,9 +83,14 @@ def load_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: line comments and blank lines are left
+    out, so an edit to comments keeps recorded counters valid."""
     h = hashlib.sha256()
     for f in sorted((ROOT / "quant_dequant_gemv_gb300" / "csrc").glob("*")):
-        h.update(f.read_bytes())
+        for line in f.read_text().splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -30,12 +30,14 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
                                  unsigned *counters, int sm_count, cudaStream_t stream);
 
 int take_status_stream();
-// Batch-1 streaming kernel (qdq_stream1.cu): takes the same packed arguments.
+// The streaming kernel (qdq_stream1.cu) at batch width bt (1, 2, 4 or 8): runs the
+// argument block packed by the plan functions above.
 int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, cudaStream_t stream);
 int take_status_stream1();
 int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);
 
-// The tensor-core batched GEMV (single GEMVs with batch >= kMmaMinBatch).
+// The tensor-core batched GEMV (single GEMVs from mma_min_batch on; it accepts any
+// batch >= kMmaMinBatch).
 int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y,
                     int batch, cudaStream_t stream, int sm_count);
 int take_status_mma();

@@ -1,5 +1,6 @@
-// qdq_stream1.cu -- fused dequant-GEMV on CUDA cores for one input vector
-// (batch 1): single GEMVs, groups and multi-level plans such as a decode step.
+// qdq_stream1.cu -- fused dequant-GEMV on CUDA cores for small batches (batch
+// widths 1, 2, 4, 8): single GEMVs, groups and multi-level plans such as a decode
+// step.
 //
 // "S21 The Capstone: picoLM, in Python", section 3 (fused dequant + dot: only the
 // quantised bytes cross the memory bus, decoded in registers into the dot
@@ -9,22 +10,26 @@
 //
 // One persistent CTA per SM, warp-specialised, with the reduction dimension
 // split across the consumer warps:
-//  * A tile is up to 16 rows x one 2048-column chunk of a GEMV. Consumer warp w
-//    owns the 256-column slice w of the chunk (one Q4_K / Q6_K super-block, eight
-//    q8_0 / q4_0 blocks) for every row of the tile: lane 4 r + c covers rows r
-//    and r + 8 and quarter c of the slice, 64 weights per row. Every warp works
-//    on every row, so even a level with a dozen rows per CTA keeps all eight
-//    warps busy, and a warp needs the x values of its slice only.
-//  * Each warp stages its own x slices (plain and/or pre-scaled copies, plus the
-//    Q4_K sub-block sums of x) into a private shared-memory area, straight from
-//    global memory once the level's inputs are ready: no CTA-wide x handshake.
-//  * A warp keeps its row partials for the whole level in a shared-memory buffer
-//    (the chunks of a row add up in place); at the end of the level (or when the
-//    buffer is full) the consumer warps meet once, add the eight partials of
-//    each row in warp order and store y.
-//  * Warp 0 streams tiles HBM -> shared memory with 1-D bulk copies into a ring
-//    of stages and fetches ahead across level boundaries (W does not depend on
-//    x). Warp 1 owns the level dependency: one device-wide counter per level.
+//  * Tiles. A whole-row tile holds up to 64 complete rows; rows too long for
+//    eight per tile, or whose x does not fit the x window, are cut into
+//    2048-column chunks of up to 32 rows. Consumer warp w owns the 256-column
+//    slices w, w + 8, ... (one Q4_K / Q6_K super-block, eight q8_0 / q4_0 blocks)
+//    for every row of the tile; lane 4 r + c covers rows r and r + 8 and quarter
+//    c of a slice, 64 weights per row, in passes of 16 rows. Every warp works on
+//    every row, so even a level with a dozen rows per CTA keeps all eight warps
+//    busy.
+//  * x. At batch width 1 each warp stages its own x slices (plain and/or
+//    pre-scaled copies, plus the Q4_K sub-block sums) into a private area and
+//    holds a slice in registers across the passes of a tile. At widths 2-8 the
+//    warps stage one CTA-wide buffer with every batch column, and each decoded
+//    weight meets every column before the next is decoded.
+//  * Partials. A warp keeps its row partials for the whole level in a
+//    shared-memory buffer (the chunks of a row add up in place); at the end of
+//    the level (or when the buffer is full) the consumer warps meet once, add
+//    the eight partials of each row in warp order and store y.
+//  * Warp 0 streams tiles HBM -> shared memory with 1-D bulk copies into a byte
+//    ring and fetches ahead across level boundaries (W does not depend on x).
+//    Warp 1 owns the level dependency: one device-wide counter per level.
 //  * Every wait is bounded (qdq_device.cuh).
 #include <cstdio>
 #include <type_traits>
