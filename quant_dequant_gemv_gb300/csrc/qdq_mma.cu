@@ -99,8 +99,18 @@ constexpr uint32_t kFinalOff = 64u * 1024u;  // per-tile result [b][128] after t
 // fit in tensor memory (Q6_K has four 16-weight groups per sub-chunk).
 __host__ __device__ constexpr int max_bpad(int type) { return type == QDQ_Q6_K ? 32 : 64; }
 __host__ __device__ constexpr int groups_per_sub(int type) { return type == QDQ_Q6_K ? 4 : 2; }
+// Padded batches up to 32 decode in four groups of four warps, each group taking
+// every fourth sub-chunk whole (see the decode warps), when tensor memory holds
+// four accumulator sets: four sub-chunks are then in flight, each in its own set.
+// A group waits for its set's MMAs with mbarrier parity; with fewer sets than
+// groups a set could be two phases ahead of a waiter, which parity cannot tell.
+// Wider batches keep all sixteen warps on every sub-chunk (three sets suffice).
+__host__ __device__ constexpr bool rr_groups(int type, int bpad) {
+    return bpad <= 32 && groups_per_sub(type) * bpad * 4 <= (int)(512 - 32 * 4);
+}
+// x_hi and x_lo stacked into one B operand when their accumulator sets still fit.
 __host__ __device__ constexpr bool stacked_b(int type, int bpad) {
-    return groups_per_sub(type) * 2 * bpad * 3 <= (int)(512 - 32 * 4);
+    return groups_per_sub(type) * 2 * bpad * (rr_groups(type, bpad) ? 4 : 3) <= (int)(512 - 32 * 4);
 }
 
 struct MmaArgs {
@@ -427,12 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < nd; ++s) {
             mbar_init(d_full + 8 * s, 1);
-            mbar_init(d_empty + 8 * s, kDecWarps);
+            mbar_init(d_empty + 8 * s, rr_groups(TYPE, BP) ? 4 : kDecWarps);
         }
-        // an A stage is full when the 16 decode warps have stored its quants and the
-        // sub-chunk's split X has landed (the X producer's arrival carries the bytes)
+        // an A stage is full when its decode warps (16, or the four of a group) have
+        // stored its quants and the sub-chunk's split X has landed (the X producer's
+        // arrival carries the bytes)
         for (int s = 0; s < kAStages; ++s) {
-            mbar_init(a_full + 8 * s, kDecWarps + 1);
+            mbar_init(a_full + 8 * s, (rr_groups(TYPE, BP) ? 4 : kDecWarps) + 1);
             mbar_init(a_empty + 8 * s, 1);
         }
         fence_mbar_init();
@@ -578,6 +589,133 @@ __global__ void __launch_bounds__(kThreads, 1)
                             rd_p ^= 1;
                         }
                     }
+                }
+            }
+        }
+    } else if constexpr (rr_groups(TYPE, BP)) {
+        // ---- decode in four groups, one warp per tensor-memory lane quarter in each:
+        // group G takes sub-chunk G of every unit (j = G, G + 4, ...), decodes all four
+        // runs of its rows into A stage G, then waits for that sub-chunk's MMAs and
+        // adds s_g Z_g (- m_g X_g) of every scale group into its rows' sums. Four
+        // sub-chunks are in flight at once, one per group.
+        const int dw = warp - kWarpDec0, G = dw >> 2;
+        const int q = warp & 3, rr = 32 * q + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+        const int rm = rr < trows ? rr % a.g : 0, rsr = rr < trows ? rr / a.g : 0;
+        const uint32_t row_off =
+            rr < trows ? (uint32_t)rm * a.region_bytes + (uint32_t)rsr * a.box_inner
+                       : (rr < rows_here ? a.left_off + (uint32_t)(rr - trows) * a.left_pitch : 0u);
+        const int64_t row_phase = rr < trows ? (int64_t)rm * a.row_bytes : (row0 + rr) * a.row_bytes;
+        float yacc[BP];  // this row's sum over the group's sub-chunks, per batch column
+#pragma unroll
+        for (int i = 0; i < BP; ++i) yacc[i] = 0.0f;
+        Ring rs(nraw);
+        bool ok = true;
+        for (int u = u0; u < u1; ++u, rs.next()) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(raw_full + 8 * rs.slot, rs.phase, status));
+            if (!ok) break;
+            const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
+            const int sub = G, n = u - u0, j = (kUnitK / kSubK) * n + sub;
+            float sg[kG], mg[kG];
+            if (sub < ns) {
+                const uint32_t stage = sb + (uint32_t)rs.slot * a.stage_bytes + row_off;
+                const int64_t unit_phase = row_phase + (int64_t)u * kUnitBytes;
+                const uint32_t blk0 = stage + (uint32_t)(unit_phase & 15);
+                const uint32_t blk1 = rr < trows ? stage + a.half_bytes + (uint32_t)((unit_phase + kKbh * kBB) & 15)
+                                                 : blk0 + kKbh * kBB;
+                if (n >= 1) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_empty + 8 * G, (n & 1) ^ 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int run = 0; run < 4; ++run) {
+                    const int h = run >> 1, p = run & 1;
+                    uint32_t blk = blk0;
+                    if constexpr (kBW == 32) {
+                        const int kb = 2 * sub + h;
+                        blk = (kb < kKbh ? blk0 : blk1) + (uint32_t)(kb & (kKbh - 1)) * kBB;
+                    }
+                    Run rn;
+                    decode_run<TYPE>(blk, sub, h, p, rn);
+                    tmem_st8(tl + 32u * G + 4 * rn.octet, rn.q);
+                    const int gi = (kG == 4) ? run : (TYPE == QDQ_Q4_K ? p : h);  // the run's scale group
+                    sg[gi] = rn.s;
+                    mg[gi] = rn.m;
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(a_full + 8 * G);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(raw_empty + 8 * rs.slot);  // this group is done with the unit's raw data
+            if (sub >= ns) continue;
+            // the sub-chunk's accumulators: set j mod nd of the MMA warp's ring. The
+            // set's previous phase (sub-chunk j - nd) is waited for first, so that the
+            // parity of this phase cannot match an older one still in flight.
+            const int ds = j % nd, dp = (j / nd) & 1;
+            if (j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp ^ 1, status));
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp, status));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int gi = 0; gi < kG; ++gi) {
+                // a group is present unless a short last sub-chunk (q8_0 / q4_0) ends first
+                const bool present = gi * (kSubK / kG) < uk - kSubK * sub;
+                const int gg = 8 * u + 2 * sub + gi;  // Q4_K: global 32-column group
+                const uint32_t dcol = tl + kDCol0 + (uint32_t)ds * dset + gi * gcols;
+#pragma unroll
+                for (int c8 = 0; c8 < BP / 8; ++c8) {
+                    uint32_t v[8];
+                    tmem_ld8(dcol + 8 * c8, v);
+                    float z[8];
+                    if constexpr (kStack) {
+                        uint32_t w[8];
+                        tmem_ld8(dcol + b_pad + 8 * c8, w);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) z[t] = __uint_as_float(v[t]) + __uint_as_float(w[t]);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) z[t] = __uint_as_float(v[t]);
+                    }
+                    if (present) {
+                        if constexpr (TYPE == QDQ_Q4_K) {
+                            const float4 *xg = reinterpret_cast<const float4 *>(a.xsum + (int64_t)gg * b_pad + 8 * c8);
+                            const float4 x0 = __ldg(xg), x1 = __ldg(xg + 1);
+                            const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                            for (int t = 0; t < 8; ++t)
+                                yacc[8 * c8 + t] = fmaf(sg[gi], z[t], fmaf(-mg[gi], xv[t], yacc[8 * c8 + t]));
+                        } else {
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) yacc[8 * c8 + t] = fmaf(sg[gi], z[t], yacc[8 * c8 + t]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(d_empty + 8 * ds);
+        }
+
+        // ---- combine the four groups of each row: slot buffer [G][n][128] at offset 0;
+        // the first barrier keeps it off raw stages that later groups may still read
+        named_bar_sync(1, kDecWarps * 32);
+        float *slotbuf = reinterpret_cast<float *>(smem);
+#pragma unroll
+        for (int b = 0; b < BP; ++b) slotbuf[(G * BP + b) * kM + rr] = yacc[b];
+        named_bar_sync(1, kDecWarps * 32);
+        if (G == 0) {
+            float *fin = reinterpret_cast<float *>(smem + kFinalOff);
+            for (int n = 0; n < a.batch; ++n) {
+                float v = 0.0f;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) v += slotbuf[(g * BP + n) * kM + rr];
+                if (S == 1) {
+                    if (rr < rows_here) a.y[(int64_t)n * a.rows + row0 + rr] = v;
+                } else {
+                    fin[n * kM + rr] = v;
                 }
             }
         }
@@ -913,7 +1051,7 @@ int ring_depths(int type, MmaArgs &a) {
     a.nx = kAStages;  // the X slots travel with the A stages
     const uint32_t dset = (uint32_t)(groups_per_sub(type) * a.b_pad * (stacked_b(type, a.b_pad) ? 2 : 1));
     a.nd = (int)std::min<uint32_t>(kMaxStages, (kTmemCols - kDCol0) / dset);
-    if (a.nd < kLag + 1) return QDQ_ERR_LIMIT;
+    if (a.nd < (rr_groups(type, a.b_pad) ? 4 : kLag + 1)) return QDQ_ERR_LIMIT;
     const Layout L0 = layout_for(a.stage_bytes, 0, a.nx, a.b_pad);
     const uint32_t fixed = L0.tmem_slot + 16u;
     a.nraw = fixed >= kSmemBudget ? 0 : (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed) / a.stage_bytes);
