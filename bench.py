@@ -82,11 +82,14 @@ def load_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(exclude=()) -> str:
     """Hash of the kernel sources' code: line comments and blank lines are left
-    out, so an edit to comments keeps recorded counters valid."""
+    out, so an edit to comments keeps recorded counters valid. `exclude` names
+    source files the recorded kernel is not built from."""
     h = hashlib.sha256()
     for f in sorted((ROOT / "quant_dequant_gemv_gb300" / "csrc").glob("*")):
+        if f.name in exclude:
+            continue
         for line in f.read_text().splitlines():
             code = line.split("//", 1)[0].rstrip()
             if code:
@@ -96,13 +99,13 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic(workload: str, batch: int):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel sources; else None."""
+    current sources of its kernel; else None."""
     p = ROOT / "profiles" / "dram_traffic.json"
     if not p.exists():
         return None
     d = json.loads(p.read_text())
     e = d.get(f"{workload}/b{batch}")
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(tuple(e.get("excluded_sources", ()))):
         return None
     return e.get("bytes_per_launch")
 

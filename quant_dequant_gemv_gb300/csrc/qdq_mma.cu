@@ -611,11 +611,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < BP; ++i) yacc[i] = 0.0f;
         Ring rs(nraw);
         bool ok = true;
+        const bool tr = q == 0 && lane == 0;  // trace builds: one warp per group records
         for (int u = u0; u < u1; ++u, rs.next()) {
+            const int sub = G, n = u - u0, j = (kUnitK / kSubK) * n + sub;
+            if (tr && n < 8) MTC(0, 8 * G + n);
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(raw_full + 8 * rs.slot, rs.phase, status));
             if (!ok) break;
             const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-            const int sub = G, n = u - u0, j = (kUnitK / kSubK) * n + sub;
             float sg[kG], mg[kG];
             if (sub < ns) {
                 const uint32_t stage = sb + (uint32_t)rs.slot * a.stage_bytes + row_off;
@@ -628,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     tc_fence_after();
                 }
+                if (tr && n < 8) MTC(1, 8 * G + n);
 #pragma unroll
                 for (int run = 0; run < 4; ++run) {
                     const int h = run >> 1, p = run & 1;
@@ -647,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(a_full + 8 * G);
+                if (tr && n < 8) MTC(2, 8 * G + n);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(raw_empty + 8 * rs.slot);  // this group is done with the unit's raw data
@@ -658,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp ^ 1, status));
             if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp, status));
             if (!ok) break;
+            if (tr && n < 8) MTC(3, 8 * G + n);
             tc_fence_after();
 #pragma unroll
             for (int gi = 0; gi < kG; ++gi) {
@@ -697,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(d_empty + 8 * ds);
+            if (tr && n < 8) MTC(4, 8 * G + n);
         }
 
         // ---- combine the four groups of each row: slot buffer [G][n][128] at offset 0;
