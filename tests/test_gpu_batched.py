@@ -27,8 +27,9 @@ def worst_rel(y, y_ref, S):
 
 
 @pytest.mark.parametrize("qtype", TYPES)
-@pytest.mark.parametrize("batch", [9, 16, 33, 64])
+@pytest.mark.parametrize("batch", [4, 5, 9, 16, 33, 64])
 def test_batched_all_formats_ragged(q, orc, qtype, batch):
+    # batch 4: q8_0 on the tensor cores, the other formats on the streaming kernel
     rows = 300  # three row tiles, the last one 44 rows
     cols = 1024 if qtype in (synth.Q4_K, synth.Q6_K) else 416  # 416 = 256 + 160: a ragged last unit
     W = synth.gen_matrix(qtype, rows, cols, 80 + batch)
