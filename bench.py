@@ -193,7 +193,7 @@ def build_inputs(levels, batch, device, seed=0):
 
 L2_BYTES = 129 * 2 ** 20   # GB300 L2
 def mma_min_batch(qtype):  # single GEMVs from this batch on run on the tensor cores (library dispatch)
-    return 4 if qtype == synth.Q8_0 else 5
+    return 4 if qtype in (synth.Q8_0, synth.Q4_0) else 5
 GROUP = 8                  # single-GEMV workloads: steps per replayed CUDA graph
 
 

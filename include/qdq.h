@@ -93,7 +93,7 @@ int qdq_dequant_async(int type, const void *blocks, int64_t n, float *out_f32,
  * gemv_q4 / gemm).
  * Accumulation is fp32. Against the exact (double) sum y_ref the result meets
  * |y - y_ref| <= 1e-5 * sum_c |w[r][c] x[b][c]| + 1e-7 for finite inputs.
- * Batch 1..4 (1..3 for q8_0) runs the streaming
+ * Batch 1..4 (1..3 for q8_0 and q4_0) runs the streaming
  * CUDA-core kernel (each decoded weight meets every batch column); larger
  * batches the tensor-core path (exact integer quants x bf16-split x on tcgen05,
  * scales applied per group in fp32). Any row width is accepted (wide rows are

@@ -60,11 +60,10 @@ constexpr int kMaxGroupDescs = 8;
 constexpr int kStreamMaxBatch = 8;  // streaming kernel (plans, groups, small single GEMVs)
 constexpr int kMmaMinBatch = 4;     // the tensor-core path takes batches from this one on
 // Single GEMVs run on the tensor cores from this batch on (measured crossover with
-// the CUDA-core streaming kernel on GB300: Q4_K, Q6_K and q4_0 stream faster up to
-// batch 4, which the streaming kernel's four-column instantiation covers; from
-// batch 5 it runs its eight-column instantiation and the tensor cores win. q8_0,
-// whose one-byte quants cost the streaming kernel most per weight, is faster on
-// the tensor cores already at batch 4).
-inline int mma_min_batch(int type) { return type == QDQ_Q8_0 ? 4 : 5; }
+// the CUDA-core streaming kernel on GB300: Q4_K and Q6_K stream faster up to batch
+// 4, which the streaming kernel's four-column instantiation covers; from batch 5 it
+// runs its eight-column instantiation and the tensor cores win. For the 32-weight
+// block formats q8_0 and q4_0 the tensor cores are faster already at batch 4).
+inline int mma_min_batch(int type) { return (type == QDQ_Q8_0 || type == QDQ_Q4_0) ? 4 : 5; }
 
 }  // namespace qdq

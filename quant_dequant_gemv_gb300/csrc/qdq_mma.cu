@@ -532,8 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kWarpMma) {
         // ---- MMA issue: the whole warp runs the loop with warp-uniform operands and
-        // one elected lane issues, so the descriptors stay in uniform registers (a
-        // lone thread issuing from per-thread registers reaches a tenth of the rate).
+        // one elected lane issues a sub-chunk's MMAs in one go, so the descriptors
+        // stay in uniform registers (a lone thread issuing from per-thread registers
+        // reaches a tenth of the rate). The two commits follow in their own elected
+        // block after a warp barrier: issued in the same block as the MMAs, a bounded
+        // wait ran out on one of the benchmark shapes.
         // Per K-step t of a sub-chunk: Z_g += q x_hi and Z_g += q x_lo into the
         // accumulator region of t's group.
         const uint32_t idesc = make_idesc(b_pad), idesc2 = make_idesc(2 * b_pad);
@@ -559,24 +562,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0 && j < 8) MTC(7, 40 + j);
                         const int ks = j == J - 1 ? ks_last : 4;
                         const uint32_t dbase = tmem + kDCol0 + (uint32_t)rd_s * dset;
+                        if (elect_one()) {
 #pragma unroll
-                        for (int t = 0; t < 4; ++t) {
-                            if (t < ks) {
-                                const uint32_t bt = xdesc_lo + s * slot_step + t * kstep_step;
-                                const uint32_t dg = dbase + ((kG == 4) ? t : (t >> 1)) * gcols;
-                                const uint32_t acc = (kG == 4) ? 0u : (uint32_t)(t & 1);  // region's first write
-                                if (elect_one()) {
+                            for (int t = 0; t < 4; ++t) {
+                                if (t < ks) {
+                                    const uint32_t bt = xdesc_lo + s * slot_step + t * kstep_step;
+                                    const uint32_t dg = dbase + ((kG == 4) ? t : (t >> 1)) * gcols;
+                                    const uint32_t acc = (kG == 4) ? 0u : (uint32_t)(t & 1);
                                     if constexpr (kStack) {
                                         mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt, xdesc_hi), idesc2, acc);
                                     } else {
                                         mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt, xdesc_hi), idesc, acc);
-                                        mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt + lo_step, xdesc_hi), idesc,
-                                               1u);
+                                        mma_ts(dg, tmem + 32u * s + 8 * t, desc_from_words(bt + lo_step, xdesc_hi), idesc, 1u);
                                     }
                                 }
-                                __syncwarp();
                             }
                         }
+                        __syncwarp();
                         if (lane == 0 && j < 8) MTC(7, 32 + j);
                         if (elect_one()) {
                             mma_commit(a_empty + 8 * s);
