@@ -65,3 +65,29 @@ def test_binding_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(qdq, "_lib", None)
     with pytest.raises(RuntimeError):
         qdq.gemv(3, 0, 1, 256, 0, 0, 1, stream=0)
+
+
+def test_group_and_plan_checks_precede_device_work(lib):
+    # Batch limits and the level sequence of a plan are checked before any device
+    # work, so these answers hold on any host.
+    import ctypes
+    assert lib.qdq_gemv_group(None, 0, 1, None) == 0                # no GEMVs: no-op
+    assert lib.qdq_gemv_group(None, 3, 0, None) == -2               # batch < 1
+    assert lib.qdq_gemv_group(None, 3, 9, None) == -8               # batch above 8
+    assert lib.qdq_gemv_group(None, -1, 1, None) == -8
+
+    def plan(levels, batch=1):
+        lv = (ctypes.c_int * max(len(levels), 1))(*levels)
+        out = ctypes.c_void_p(12345)
+        rc = lib.qdq_plan_create(None, lv, len(levels), batch, ctypes.byref(out))
+        assert out.value is None                                    # no plan on failure
+        return rc
+
+    assert plan([0, 1], batch=0) == -2
+    assert plan([0, 1], batch=9) == -8
+    assert plan([1, 1]) == -2                                       # must start at level 0
+    assert plan([0, 2]) == -2                                       # levels go up one at a time
+    assert plan([0, 1, 0]) == -2                                    # and never down
+    assert plan(list(range(129))) == -8                             # more than 128 levels
+    assert plan([0] * 193) == -8                                    # more than 192 GEMVs
+    assert plan([]) == -8
