@@ -23,12 +23,15 @@
 //               (L2 evict-first);
 //   warp 1      owns the tensor memory; its elected lane issues the MMAs;
 //   warp 2      copies the split X of each 64-column sub-chunk into a ring;
-//   warps 3-18  thread (row, run) turns a run of 16 consecutive quants of its row
-//               per sub-chunk into exact bf16 (a byte permute puts each quant
-//               under the bf16 exponent of 128, a bf16 subtraction removes the
-//               offset) and stores them to tensor memory; two sub-chunks later
-//               the same thread reads its group's accumulator back and adds
-//               s_g Z_g (- m_g X_g) into registers.
+//   warps 3-18  turn quants into exact bf16 (a byte permute puts each quant under
+//               the bf16 exponent of 128, a bf16 subtraction removes the offset),
+//               store them to tensor memory and later read the group
+//               accumulators back, adding s_g Z_g (- m_g X_g) into registers.
+//               Padded batches up to 32: four groups of four warps (one per
+//               tensor-memory lane quarter), group G taking every fourth 64-column
+//               sub-chunk whole, so four sub-chunks are in flight. Wider batches:
+//               thread (row, run) decodes one 16-quant run of every sub-chunk and
+//               reads its accumulator two sub-chunks later.
 // Split-K: the CTAs that share a row tile form a thread-block cluster along K.
 // Each leaves its partial tile in shared memory and the cluster sums the
 // partials through distributed shared memory in rank order, so y is
