@@ -75,6 +75,33 @@ static int check_gemv_ptrs(const void *W, const float *x, float *y, int device) 
     return rc;
 }
 
+// Descriptors of a group or plan: shapes, pointers, and agreement on shared x.
+int check_descs(const qdq_gemv_desc *descs, int n, int batch, int device) {
+    if (descs == nullptr || n < 0) return QDQ_ERR_PTR;
+    for (int i = 0; i < n; ++i) {
+        int rc = check_gemv_shape(descs[i].type, descs[i].rows, descs[i].cols, batch);
+        if (rc) return rc;
+        if (descs[i].rows == 0 || descs[i].cols == 0) return QDQ_ERR_SHAPE;
+        if ((rc = check_gemv_ptrs(descs[i].W, descs[i].x, descs[i].y, device))) return rc;
+    }
+    // GEMVs that read the same x must agree on its length
+    for (int i = 0; i < n; ++i)
+        for (int k = 0; k < i; ++k)
+            if (descs[k].x == descs[i].x && descs[k].cols != descs[i].cols) return QDQ_ERR_SHAPE;
+    return QDQ_OK;
+}
+
+
+// Level indices of a plan: start at 0 and never skip or go back. *nlevels gets
+// the level count; more than max_levels gives QDQ_ERR_LIMIT.
+int check_levels(const int *level, int n, int max_levels, int *nlevels) {
+    if (level[0] != 0) return QDQ_ERR_SHAPE;
+    for (int i = 1; i < n; ++i)
+        if (level[i] != level[i - 1] && level[i] != level[i - 1] + 1) return QDQ_ERR_SHAPE;
+    *nlevels = level[n - 1] + 1;
+    return *nlevels > max_levels ? QDQ_ERR_LIMIT : QDQ_OK;
+}
+
 }  // namespace qdq
 
 using namespace qdq;
@@ -180,21 +207,6 @@ int qdq_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x
     return run_stream_once(&d, 1, batch, s, dev.sm_count);
 }
 
-static int check_descs(const qdq_gemv_desc *descs, int n, int batch, int device) {
-    if (descs == nullptr || n < 0) return QDQ_ERR_PTR;
-    for (int i = 0; i < n; ++i) {
-        int rc = check_gemv_shape(descs[i].type, descs[i].rows, descs[i].cols, batch);
-        if (rc) return rc;
-        if (descs[i].rows == 0 || descs[i].cols == 0) return QDQ_ERR_SHAPE;
-        if ((rc = check_gemv_ptrs(descs[i].W, descs[i].x, descs[i].y, device))) return rc;
-    }
-    // GEMVs that read the same x must agree on its length
-    for (int i = 0; i < n; ++i)
-        for (int k = 0; k < i; ++k)
-            if (descs[k].x == descs[i].x && descs[k].cols != descs[i].cols) return QDQ_ERR_SHAPE;
-    return QDQ_OK;
-}
-
 int qdq_gemv_group(const qdq_gemv_desc *descs, int n, int batch, qdq_stream_t stream) {
     if (n == 0) return QDQ_OK;
     if (n < 0 || n > kMaxGroupDescs) return QDQ_ERR_LIMIT;
@@ -213,12 +225,9 @@ int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int bat
     if (n < 1 || n > kMaxPlanDescs) return QDQ_ERR_LIMIT;
     if (batch < 1) return QDQ_ERR_SHAPE;
     if (batch > kStreamMaxBatch) return QDQ_ERR_LIMIT;
-    if (level[0] != 0) return QDQ_ERR_SHAPE;
-    for (int i = 1; i < n; ++i)
-        if (level[i] != level[i - 1] && level[i] != level[i - 1] + 1) return QDQ_ERR_SHAPE;
-    const int nlevels = level[n - 1] + 1;
-    if (nlevels > kMaxPlanLevels) return QDQ_ERR_LIMIT;
-    int rc;
+    int nlevels = 0;
+    int rc = check_levels(level, n, kMaxPlanLevels, &nlevels);
+    if (rc) return rc;
     const DeviceInfo &dev = current_device(&rc);
     if (rc) return rc;
     if ((rc = check_descs(descs, n, batch, dev.device))) return rc;

@@ -42,6 +42,21 @@ QDQ_DEV void q4k_pair_fields(uint32_t H1, uint32_t H2, uint32_t H3, int c, uint3
     *mn = (b & 0x0F0Fu) | (((H2 >> sh) >> top) & 0x3030u);
 }
 
+// Recentering of a Q4_K sub-block for the factored dot product. With s = d sc and
+// m = dmin mn (both exact in fp32: an 11-bit fp16 significand times a 6-bit field),
+// every weight is w = s q - m, q in 0..15. Summing s (q - rho) x - (m - s rho) x over
+// the sub-block, with rho the integer in [0, 15] nearest to m / s, keeps both
+// factored terms within a small multiple of sum |w x|: |m - s rho| <= |s| / 2, and
+// m - s rho is exact (Sterbenz) whenever rho is not clamped. Without it, a sub-block
+// whose weights nearly cancel (s q close to m) would lose the result to rounding.
+// Returns rho; *m_rest = m - s rho. Degenerate s (zero, non-finite ratio) gives
+// rho = 0 or 15 and the plain form.
+QDQ_DEV float q4k_center(float s, float m, float *m_rest) {
+    const float rho = fminf(fmaxf(rintf(__fdividef(m, s)), 0.0f), 15.0f);
+    *m_rest = fmaf(-s, rho, m);
+    return rho;
+}
+
 // ---- Q6_K -------------------------------------------------------------------------
 // Given the ql word holding bytes l..l+3 of the run used by k (run k&1) and the qh
 // word holding bytes l..l+3 of qh's half, returns the four 6-bit quants q6 of

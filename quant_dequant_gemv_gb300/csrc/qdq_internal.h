@@ -17,6 +17,11 @@ struct DeviceInfo {
 // Cached per device; ok == false when the current device is not sm_103.
 const DeviceInfo &current_device(int *status);
 
+// Argument checks shared by every entry point that takes GEMV descriptors
+// (qdq_api.cu): shapes and device pointers, and the plan level sequence.
+int check_descs(const qdq_gemv_desc *descs, int n, int batch, int device);
+int check_levels(const int *level, int n, int max_levels, int *nlevels);
+
 int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStream_t stream, int sm_count);
 
 // The streaming (CUDA-core) GEMV over a list of GEMVs grouped in dependency levels.

@@ -265,20 +265,25 @@ struct Run {
 
 // Q4_K: chunk `sub` holds sub-blocks 2 sub (low nibbles) and 2 sub + 1 (high
 // nibbles); half h takes bytes 16h..16h+15 of the chunk, p picks the nibble, so
-// the group is sub-block 2 sub + p with s = d sc, m = dmin mn.
+// the group is sub-block 2 sub + p with s = d sc, m = dmin mn. The group is
+// recentred (q4k_center): the A operand holds q - rho and the epilogue subtracts
+// (m - s rho) X_g, so that both terms stay within a small multiple of sum |w x|.
 QDQ_DEV void run_q4k(uint32_t blk, int sub, int h, int p, Run &o) {
     const uint4 H = lds128(blk);
     const uint4 V = lds128(blk + 16 + 32 * sub + 16 * h);
     uint32_t sc2, mn2;
     q4k_pair_fields(H.y, H.z, H.w, sub, &sc2, &mn2);
     o.s = __fmul_rn(half_bits_to_float(H.x & 0xFFFF), (float)((sc2 >> (8 * p)) & 0xFF));
-    o.m = __fmul_rn(half_bits_to_float(H.x >> 16), (float)((mn2 >> (8 * p)) & 0xFF));
+    const float m = __fmul_rn(half_bits_to_float(H.x >> 16), (float)((mn2 >> (8 * p)) & 0xFF));
+    const uint32_t rho = (uint32_t)q4k_center(o.s, m, &o.m);
+    const uint32_t off16 = 0x4300u + rho;  // the bf16 128 + rho (exact: rho <= 15)
+    const uint32_t off = off16 | (off16 << 16);
     const uint32_t v[4] = {V.x, V.y, V.z, V.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t nib = (v[i] >> (4 * p)) & 0x0F0F0F0Fu;
-        o.q[2 * i] = bf16x2_sub(bf16_biased_pair(nib, 0x4140), kBf16x2_128);
-        o.q[2 * i + 1] = bf16x2_sub(bf16_biased_pair(nib, 0x4342), kBf16x2_128);
+        o.q[2 * i] = bf16x2_sub(bf16_biased_pair(nib, 0x4140), off);
+        o.q[2 * i + 1] = bf16x2_sub(bf16_biased_pair(nib, 0x4342), off);
     }
     o.octet = p == 0 ? 2 * h : 4 + 2 * h;
 }

@@ -40,18 +40,6 @@ static int counters_for_device(int device, unsigned **out) {
     return QDQ_OK;
 }
 
-static int check_ptr(const void *p, int device) {
-    if (p == nullptr) return QDQ_ERR_PTR;
-    cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
-        cudaGetLastError();
-        return QDQ_ERR_PTR;
-    }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return QDQ_ERR_PTR;
-    if (attr.type == cudaMemoryTypeDevice && attr.device != device) return QDQ_ERR_PTR;
-    return ((uintptr_t)p & 15) ? QDQ_ERR_ALIGN : QDQ_OK;
-}
-
 }  // namespace qdq
 
 using namespace qdq;
@@ -62,26 +50,12 @@ extern "C" int qdq_gemv_levels_noalloc(const qdq_gemv_desc *descs, const int *le
     if (n < 1 || n > kMaxPlanDescs) return QDQ_ERR_LIMIT;
     if (batch < 1) return QDQ_ERR_SHAPE;
     if (batch > kStreamMaxBatch) return QDQ_ERR_LIMIT;
-    if (level[0] != 0) return QDQ_ERR_SHAPE;
-    for (int i = 1; i < n; ++i)
-        if (level[i] != level[i - 1] && level[i] != level[i - 1] + 1) return QDQ_ERR_SHAPE;
-    const int nlevels = level[n - 1] + 1;
-    if (nlevels > kNoAllocMaxLevels) return QDQ_ERR_LIMIT;
-    int rc;
+    int nlevels = 0;
+    int rc = check_levels(level, n, kNoAllocMaxLevels, &nlevels);
+    if (rc) return rc;
     const DeviceInfo &dev = current_device(&rc);
     if (rc) return rc;
-    for (int i = 0; i < n; ++i) {
-        const qdq_gemv_desc &d = descs[i];
-        const int qk = qdq_block_weights(d.type);
-        if (qk < 0) return QDQ_ERR_TYPE;
-        if (d.rows < 1 || d.cols < 1 || d.cols % qk || d.rows > ((int64_t)1 << 40) || d.cols > ((int64_t)1 << 30))
-            return QDQ_ERR_SHAPE;
-        if ((rc = check_ptr(d.W, dev.device)) || (rc = check_ptr(d.x, dev.device)) ||
-            (rc = check_ptr(d.y, dev.device)))
-            return rc;
-        for (int k = 0; k < i; ++k)
-            if (descs[k].x == d.x && descs[k].cols != d.cols) return QDQ_ERR_SHAPE;
-    }
+    if ((rc = check_descs(descs, n, batch, dev.device))) return rc;
     unsigned *counters = nullptr;
     if ((rc = counters_for_device(dev.device, &counters))) return rc;
     cudaStream_t s = (cudaStream_t)stream;

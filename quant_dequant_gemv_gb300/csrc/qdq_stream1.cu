@@ -484,6 +484,7 @@ QDQ_DEV void xpairs_b(const float *xs, int b, int u, uint64_t &p0, uint64_t &p1)
 }
 
 // Q4_K, NR rows x BT columns: each word is decoded once and meets every column.
+// Sub-blocks are recentred as in unit_q4k (q4k_center).
 template <int NR, int BT>
 QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const float *sums, float (&out)[NR][BT]) {
     uint4 H[NR], Qa[NR], Qb[NR];
@@ -493,7 +494,21 @@ QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const 
         Qa[r] = ld4(wrow[r] + 16 + 32 * c);
         Qb[r] = ld4(wrow[r] + 32 + 32 * c);
     }
-    const uint64_t M2 = bits2(__float_as_uint(kTwo23), __float_as_uint(kTwo23));
+    float s_lo[NR], s_hi[NR], m_lo[NR], m_hi[NR];
+    uint64_t C_a[NR], C_b[NR], C_h[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        uint32_t sc2, mn2;
+        q4k_pair_fields(H[r].y, H[r].z, H[r].w, c, &sc2, &mn2);
+        const float d = half_bits_to_float(H[r].x & 0xFFFF), dmin = half_bits_to_float(H[r].x >> 16);
+        s_lo[r] = d * (float)(sc2 & 0xFF);
+        s_hi[r] = d * (float)(sc2 >> 8);
+        const float r_lo = q4k_center(s_lo[r], dmin * (float)(mn2 & 0xFF), &m_lo[r]);
+        const float r_hi = q4k_center(s_hi[r], dmin * (float)(mn2 >> 8), &m_hi[r]);
+        C_a[r] = pack2(fmaf(r_lo, 1.0f, kTwo23), fmaf(r_lo, 256.0f, kTwo23));
+        C_b[r] = pack2(fmaf(r_lo, 65536.0f, kTwo23), fmaf(r_lo, 256.0f, kTwo23));
+        C_h[r] = pack2(fmaf(r_hi, 16.0f, kTwo23), fmaf(r_hi, 4096.0f, kTwo23));
+    }
     uint64_t lo[NR][BT], hi[NR][BT];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
@@ -506,10 +521,10 @@ QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const 
         for (int r = 0; r < NR; ++r) {
             const uint32_t w[8] = {Qa[r].x, Qa[r].y, Qa[r].z, Qa[r].w, Qb[r].x, Qb[r].y, Qb[r].z, Qb[r].w};
             const uint32_t v = w[t], u = v >> 16;
-            q0[r] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2);
-            q1[r] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2);
-            q2[r] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2);
-            q3[r] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2);
+            q0[r] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), C_a[r]);
+            q1[r] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), C_b[r]);
+            q2[r] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), C_h[r]);
+            q3[r] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), C_h[r]);
         }
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
@@ -525,14 +540,11 @@ QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const 
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-        uint32_t sc2, mn2;
-        q4k_pair_fields(H[r].y, H[r].z, H[r].w, c, &sc2, &mn2);
-        const float d = half_bits_to_float(H[r].x & 0xFFFF), dmin = half_bits_to_float(H[r].x >> 16);
-        const float sl = (float)(sc2 & 0xFF), sh = (float)(sc2 >> 8), ml = (float)(mn2 & 0xFF), mh = (float)(mn2 >> 8);
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
             const float l = lo_of(lo[r][b]) + hi_of(lo[r][b]), h = lo_of(hi[r][b]) + hi_of(hi[r][b]);
-            out[r][b] = d * (sl * l + sh * h) - dmin * (ml * sums[b * 64 + 2 * c] + mh * sums[b * 64 + 2 * c + 1]);
+            out[r][b] = (s_lo[r] * l + s_hi[r] * h) -
+                        (m_lo[r] * sums[b * 64 + 2 * c] + m_hi[r] * sums[b * 64 + 2 * c + 1]);
         }
     }
 }

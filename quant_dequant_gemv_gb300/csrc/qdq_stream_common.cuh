@@ -103,8 +103,12 @@ QDQ_DEV void ld_words_a2(const uint8_t *p, uint32_t (&out)[N]) {
 }
 
 // Q4_K: lane = 4 s + c covers chunk c of super-block s: sub-block 2c (low nibbles,
-// x[0..31] of the slice) and 2c+1 (high nibbles, x[32..63]).
-// sum = d * (sc_lo * sum(q x)_lo + sc_hi * sum(q x)_hi) - dmin * (mn_lo * sum(x)_lo + mn_hi * sum(x)_hi)
+// x[0..31] of the slice) and 2c+1 (high nibbles, x[32..63]). Each sub-block is
+// recentred (q4k_center): with s = d sc, m = dmin mn and rho its integer offset,
+// sum = s_lo * sum((q - rho_lo) x)_lo + s_hi * sum((q - rho_hi) x)_hi
+//       - (m_lo - s_lo rho_lo) * sum(x)_lo - (m_hi - s_hi rho_hi) * sum(x)_hi.
+// A nibble left at bit position p reads as 2^23 + q 2^p; subtracting 2^23 + rho 2^p
+// leaves (q - rho) 2^p exactly, against x pre-scaled by 2^-p.
 template <int NR>
 QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, float (&out)[NR]) {
     const int s = lane >> 2, c = lane & 3;
@@ -116,27 +120,32 @@ QDQ_DEV void unit_q4k(const uint8_t *const *wrow, int lane, const XSlice &xr, fl
         Qa[r] = ld4(sb + 16 + 32 * c);
         Qb[r] = ld4(sb + 32 + 32 * c);
     }
-    const uint64_t M2 = bits2(__float_as_uint(kTwo23), __float_as_uint(kTwo23));
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         uint32_t sc2, mn2;
         q4k_pair_fields(H[r].y, H[r].z, H[r].w, c, &sc2, &mn2);
         const float d = half_bits_to_float(H[r].x & 0xFFFF), dmin = half_bits_to_float(H[r].x >> 16);
-        const float sc_lo = (float)(sc2 & 0xFF), sc_hi = (float)(sc2 >> 8);
-        const float mn_lo = (float)(mn2 & 0xFF), mn_hi = (float)(mn2 >> 8);
+        const float s_lo = d * (float)(sc2 & 0xFF), s_hi = d * (float)(sc2 >> 8);
+        float m_lo, m_hi;
+        const float r_lo = q4k_center(s_lo, dmin * (float)(mn2 & 0xFF), &m_lo);
+        const float r_hi = q4k_center(s_hi, dmin * (float)(mn2 >> 8), &m_hi);
+        // 2^23 + rho 2^p for the nibble positions of each pair (0, 8), (16, 8), (4, 12)
+        const uint64_t C_a = pack2(fmaf(r_lo, 1.0f, kTwo23), fmaf(r_lo, 256.0f, kTwo23));
+        const uint64_t C_b = pack2(fmaf(r_lo, 65536.0f, kTwo23), fmaf(r_lo, 256.0f, kTwo23));
+        const uint64_t C_h = pack2(fmaf(r_hi, 16.0f, kTwo23), fmaf(r_hi, 4096.0f, kTwo23));
         const uint32_t w[8] = {Qa[r].x, Qa[r].y, Qa[r].z, Qa[r].w, Qb[r].x, Qb[r].y, Qb[r].z, Qb[r].w};
         uint64_t a0 = 0, a1 = 0, h0 = 0, h1 = 0;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             const uint32_t v = w[t], u = v >> 16;
-            a0 = ffma2(fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), M2), xr.v[2 * t], a0);
-            a1 = ffma2(fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), M2), xr.v[2 * t + 1], a1);
-            h0 = ffma2(fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), M2), xr.v[16 + 2 * t], h0);
-            h1 = ffma2(fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), M2), xr.v[17 + 2 * t], h1);
+            a0 = ffma2(fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), C_a), xr.v[2 * t], a0);
+            a1 = ffma2(fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), C_b), xr.v[2 * t + 1], a1);
+            h0 = ffma2(fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), C_h), xr.v[16 + 2 * t], h0);
+            h1 = ffma2(fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), C_h), xr.v[17 + 2 * t], h1);
         }
         const float lo = (lo_of(a0) + hi_of(a0)) + (lo_of(a1) + hi_of(a1));
         const float hi = (lo_of(h0) + hi_of(h0)) + (lo_of(h1) + hi_of(h1));
-        out[r] = d * (sc_lo * lo + sc_hi * hi) - dmin * (mn_lo * xr.s0 + mn_hi * xr.s1);
+        out[r] = (s_lo * lo + s_hi * hi) - (m_lo * xr.s0 + m_hi * xr.s1);
     }
 }
 

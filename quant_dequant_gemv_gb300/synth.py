@@ -75,6 +75,41 @@ def gen_blocks(qtype: int, nblocks: int, rng: np.random.Generator) -> np.ndarray
     return out.reshape(-1)
 
 
+def gen_blocks_full_range(qtype: int, nblocks: int, rng: np.random.Generator) -> np.ndarray:
+    """Uniform random bytes in every field of every block, except that the scales
+    stay finite and bounded: an fp16 scale (Q4_K d and dmin, Q6_K d, q4_0 d) whose
+    exponent field is all ones (inf/NaN) gets exponent 30 instead, and the fp32
+    scale of q8_0 keeps an exponent field of at most 200 (|d| < 2^74), so that no
+    dot product over a row overflows fp32. Everything else covers its full range:
+    negative, subnormal and zero scales, 6-bit Q4_K scales and mins 0..63, int8
+    Q6_K scales down to -128, q8_0 quants down to -128."""
+    bb = BLOCK_BYTES[qtype]
+    out = rng.integers(0, 256, (nblocks, bb), dtype=np.uint8)
+
+    def clamp_fp16(col: int) -> None:
+        h = out[:, col].astype(np.uint16) | (out[:, col + 1].astype(np.uint16) << 8)
+        inf_nan = ((h >> 10) & 31) == 31
+        h = np.where(inf_nan, h & ~np.uint16(0x0400), h)
+        out[:, col] = (h & 0xFF).astype(np.uint8)
+        out[:, col + 1] = (h >> 8).astype(np.uint8)
+
+    if qtype == Q4_K:
+        clamp_fp16(0)
+        clamp_fp16(2)
+    elif qtype == Q6_K:
+        clamp_fp16(208)
+    elif qtype == Q4_0:
+        clamp_fp16(0)
+    elif qtype == Q8_0:
+        w = out[:, 0:4].copy().view("<u4").reshape(-1)
+        e = (w >> 23) & 0xFF
+        w = np.where(e > 200, (w & ~np.uint32(0x7F800000)) | np.uint32(200 << 23), w)
+        out[:, 0:4] = w.astype("<u4").view(np.uint8).reshape(-1, 4)
+    else:
+        raise ValueError(f"unknown block type {qtype}")
+    return out.reshape(-1)
+
+
 def gen_matrix(qtype: int, rows: int, cols: int, seed: int) -> np.ndarray:
     """A rows x cols weight matrix: row-major, each row a run of whole blocks."""
     if cols % BLOCK_WEIGHTS[qtype]:

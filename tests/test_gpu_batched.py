@@ -1,8 +1,10 @@
 """GPU parity of the batched (tensor-core) GEMV path, batch >= 9, against the oracle.
 
-The batched path splits every weight and activation into two bf16 terms and
-accumulates w_hi x_hi + w_hi x_lo + w_lo x_hi in fp32; it must meet the same
-per-output bound as the streaming path, |y - y_ref| <= 1e-5 * sum|w x| + 1e-7.
+The batched path multiplies each scale group's integer quants (exact in bf16,
+recentred for Q4_K) by x split into bf16 hi + lo terms, accumulates the group
+sums in fp32 in tensor memory and applies the group's scale (and, for Q4_K, its
+min) in fp32; it must meet the same per-output bound as the streaming path,
+|y - y_ref| <= 1e-5 * sum|w x| + 1e-7.
 The cases cover every format, ragged row tiles, ragged K (q8_0/q4_0 widths
 that are not a multiple of 256), split-K clusters of 1 to 8 CTAs, batches past
 one 128-wide chunk, a matrix whose byte length is not a multiple of 16, and
