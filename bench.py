@@ -10,7 +10,8 @@ exceed the 129 MB L2 several times over, so no flush is needed between steps.
 Prints one JSON line. `value` is HBM GB/s of algorithmic bytes (weights + x + y
 per step) over the device-timed step; `tok_s` is steps per second.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload step|q4k|q6k|ffn_q4k|ffn_q6k|q8_0|q4_0] [--batch B]
+                  [--workload step|q4k|q6k|ffn_q4k|ffn_q6k|q8_0|q4_0|dequant_q4k|dequant_q6k|
+                              dequant_q8_0|dequant_q4_0] [--batch B]
 Under torchrun each rank runs an independent replica (the path has no data
 exchange); rank 0 prints the aggregate.
 """
@@ -46,10 +47,19 @@ WORKLOADS = {
     "ffn_q6k": "Q6_K GEMV 2048x5632 (ffn_down shape)",
     "q8_0": "PETIT q8_0 GEMVs 14336x4096 and 4096x14336",
     "q4_0": "PETIT q4_0 GEMVs 14336x4096 and 4096x14336",
+    "dequant_q4k": "standalone dequantisation, Q4_K, 2^27 weights -> fp32",
+    "dequant_q6k": "standalone dequantisation, Q6_K, 2^27 weights -> fp32",
+    "dequant_q8_0": "standalone dequantisation, PETIT q8_0, 2^27 weights -> fp32",
+    "dequant_q4_0": "standalone dequantisation, PETIT q4_0, 2^27 weights -> fp32",
 }
+DEQUANT_TYPES = {"dequant_q4k": synth.Q4_K, "dequant_q6k": synth.Q6_K, "dequant_q8_0": synth.Q8_0,
+                 "dequant_q4_0": synth.Q4_0}
+DEQUANT_N = 1 << 27  # weights per dequantisation step: in + out bytes are several times L2
 
 
 def workload_levels(name: str, layers: int = 22) -> list[list[synth.Gemv]]:
+    if name in DEQUANT_TYPES:
+        return []
     if name == "step":
         return synth.llama_1b_step(layers)
     if name == "q4k":
@@ -64,6 +74,11 @@ def workload_levels(name: str, layers: int = 22) -> list[list[synth.Gemv]]:
         t = synth.Q8_0 if name == "q8_0" else synth.Q4_0
         return [[synth.Gemv("w_up", t, 14336, 4096)], [synth.Gemv("w_down", t, 4096, 14336)]]
     raise SystemExit(f"unknown workload {name}")
+
+
+def dequant_bytes(qtype: int, n: int) -> int:
+    """Standalone dequantisation: the blocks read once, n floats written once."""
+    return n // synth.BLOCK_WEIGHTS[qtype] * synth.BLOCK_BYTES[qtype] + 4 * n
 
 
 def algorithmic_bytes(levels, batch: int) -> int:
@@ -203,6 +218,79 @@ def gemv_launches(g, batch):
         return 1
     per = 32 if g.qtype == synth.Q6_K else 64
     return 2 * ((batch + per - 1) // per)  # split-x kernel + tensor-core kernel per batch slice
+
+
+def run_dequant(args, device):
+    """Standalone dequantisation: one qdq_dequant call per step on 2^27 weights
+    (blocks and output exceed L2, so no flush is needed)."""
+    import torch
+    from quant_dequant_gemv_gb300 import build, qdq
+
+    build.build()
+    qtype = DEQUANT_TYPES[args.workload]
+    n = DEQUANT_N
+    blocks_host = synth.gen_blocks(qtype, n // synth.BLOCK_WEIGHTS[qtype], np.random.default_rng(0))
+    blocks = torch.from_numpy(blocks_host).to(device)
+    out = torch.empty(n, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        qdq.dequant(qtype, blocks, n, out, stream)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    t_load = time.perf_counter()
+    while time.perf_counter() - t_load < 1.0:
+        for _ in range(20):
+            qdq.dequant(qtype, blocks, n, out, stream)
+        torch.cuda.synchronize(device)
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for e in evs:
+        e[0].record(stream)
+        qdq.dequant(qtype, blocks, n, out, stream)
+        e[1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    rc = qdq.get_device_status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status after timing: {qdq.status_string(rc)}")
+    # end to end: pinned host blocks in, fp32 weights out, every step
+    b_pin = torch.from_numpy(blocks_host).pin_memory()
+    o_pin = torch.empty(n, dtype=torch.float32).pin_memory()
+    E = 3
+    te = time.perf_counter()
+    for _ in range(E):
+        blocks.copy_(b_pin, non_blocking=True)
+        qdq.dequant(qtype, blocks, n, out, stream)
+        o_pin.copy_(out, non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - te) / E
+    return {"total_ms": t0.elapsed_time(t1), "launch_ms": [a.elapsed_time(b) for a, b in evs],
+            "abytes": dequant_bytes(qtype, n), "clocks": clocks, "e2e_s": e2e_s,
+            "h2d": b_pin.numel(), "d2h": 4 * n, "launches": K}
+
+
+def dequant_cpu_baseline(workload: str, budget_s: float = 8.0) -> dict:
+    """The oracle's dequantisation on the host, one thread, on 2^22-weight samples."""
+    import oracle
+    orc = oracle.get()
+    qtype = DEQUANT_TYPES[workload]
+    n = 1 << 22
+    blocks = synth.gen_blocks(qtype, n // synth.BLOCK_WEIGHTS[qtype], np.random.default_rng(0))
+    spent, reps = 0.0, 0
+    while spent < budget_s:
+        ts = time.perf_counter()
+        orc.dequant(qtype, blocks, n)
+        spent += time.perf_counter() - ts
+        reps += 1
+    return {"value": round(reps * dequant_bytes(qtype, n) / spent / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle", **host_cpu(),
+            "sample": f"{reps} dequantisations of 2^22 weights ({spent:.1f} s), plain C oracle, one thread"}
 
 
 def run_ours(args, rank, world, device):
@@ -369,23 +457,87 @@ def run_ours(args, rank, world, device):
             "e2e_s": e2e_s, "h2d": h2d, "d2h": d2h, "launches": K * launches_per_step}
 
 
-def time_oracle(levels, batch, budget_s):
-    """Time only the oracle calls (input generation excluded)."""
+def host_cpu() -> dict:
+    """Host core count and CPU model, for the CPU baseline record."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip() == "Model name":
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None:
+        try:
+            for line in Path("/proc/cpuinfo").read_text().splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    import platform
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.processor() or platform.machine()}
+
+
+def time_oracle(levels, batch, budget_s, mode="single", threads=1):
+    """Time the CPU baseline on the workload's GEMVs in step order, until budget_s
+    of measured time is spent (input generation excluded). Modes:
+      single  -- the C oracle, one thread (dequantise a row, dot in double);
+      threads -- the same C oracle, the rows of each GEMV split over `threads`
+                 host threads (ctypes releases the GIL during the C call);
+      numpy   -- unfused: the C oracle dequantises the whole matrix to fp32, then
+                 a NumPy matmul (BLAS) multiplies it by x, the dequantise-per-call
+                 structure of the NumPy port the pages describe.
+    Returns (seconds, bytes of the GEMVs done, GEMVs done)."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     orc = oracle.get()
+    pool = ThreadPoolExecutor(max_workers=threads) if mode == "threads" else None
     spent, done_bytes, n = 0.0, 0, 0
-    for li, level in enumerate(levels):
-        x = synth.gen_x(batch, level[0].cols, 1000 + li)
-        for gi, g in enumerate(level):
-            W = synth.gen_matrix(g.qtype, g.rows, g.cols, 10 * li + gi)
-            ts = time.perf_counter()
-            orc.gemv(g.qtype, W, g.rows, g.cols, x)
-            spent += time.perf_counter() - ts
-            done_bytes += g.weight_bytes + 4 * batch * (g.cols + g.rows)
-            n += 1
-        if spent > budget_s:
-            break
+    try:
+        for li, level in enumerate(levels):
+            x = synth.gen_x(batch, level[0].cols, 1000 + li)
+            for gi, g in enumerate(level):
+                W = synth.gen_matrix(g.qtype, g.rows, g.cols, 10 * li + gi)
+                ts = time.perf_counter()
+                if mode == "single":
+                    orc.gemv(g.qtype, W, g.rows, g.cols, x)
+                elif mode == "threads":
+                    bounds = [g.rows * t // threads for t in range(threads + 1)]
+                    list(pool.map(lambda t: orc.gemv(g.qtype, W, g.rows, g.cols, x, bounds[t], bounds[t + 1]),
+                                  range(threads)))
+                else:
+                    Wf = orc.dequant(g.qtype, W, g.rows * g.cols).reshape(g.rows, g.cols)
+                    np.matmul(x, Wf.T)
+                spent += time.perf_counter() - ts
+                done_bytes += g.weight_bytes + 4 * batch * (g.cols + g.rows)
+                n += 1
+            if spent > budget_s:
+                break
+    finally:
+        if pool is not None:
+            pool.shutdown()
     return spent, done_bytes, n
+
+
+def cpu_baselines(levels, batch, budget_single=10.0, budget_other=5.0) -> dict:
+    """The three CPU baselines side by side (reported only, never targets)."""
+    cpu = host_cpu()
+    threads = cpu["host_cores"] or 1
+    legs = {}
+    for name, mode, th, budget in (("oracle_1_thread", "single", 1, budget_single),
+                                   ("oracle_all_cores", "threads", threads, budget_other),
+                                   ("numpy_unfused", "numpy", 1, budget_other)):
+        spent, done, n = time_oracle(levels, batch, budget, mode, th)
+        legs[name] = {"value": round(done / spent / 1e9, 4), "unit": "GB/s",
+                      "threads": th if mode != "numpy" else "dequantise: 1; matmul: NumPy's BLAS threads",
+                      "sample": f"first {n} GEMVs of the workload in step order ({done / 1e6:.0f} MB of weights, "
+                                f"{spent:.1f} s)"}
+    first = legs["oracle_1_thread"]
+    return {"value": first["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "oracle_1_thread leg: " + first["sample"] + "; plain C oracle, one thread",
+            **cpu, "legs": legs}
 
 
 def slowest_replica(total_ms: float, e2e_s: float, world: int, device) -> tuple[float, float]:
@@ -424,7 +576,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     levels = workload_levels(args.workload, args.layers)
-    abytes = algorithmic_bytes(levels, args.batch)
+    abytes = (dequant_bytes(DEQUANT_TYPES[args.workload], DEQUANT_N) if args.workload in DEQUANT_TYPES
+              else algorithmic_bytes(levels, args.batch))
     step_bytes = abytes
     wname = WORKLOADS[args.workload]
     tkey = args.workload
@@ -437,6 +590,16 @@ def main():
         # each step is a bounded sample of the workload (its first GEMVs in step
         # order, about 1 s of work); the metric is extrapolated per byte.
         if rank != 0:
+            return
+        if args.workload in DEQUANT_TYPES:
+            cpu = dequant_cpu_baseline(args.workload, budget_s=0.5 * args.steps)
+            line = {"impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "GB/s",
+                    "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": round(1e3 * step_bytes / (cpu["value"] * 1e9), 3), "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                    "config": {"workload": wname, "l2": "n/a (CPU)"}, "cpu_baseline": cpu,
+                    "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(line))
             return
         budget = 0.8
         for _ in range(args.warmup):
@@ -469,7 +632,7 @@ def main():
         dist.init_process_group("nccl")
     device = torch.device(f"cuda:{local}")
     torch.cuda.set_device(device)
-    r = run_ours(args, rank, world, device)
+    r = run_dequant(args, device) if args.workload in DEQUANT_TYPES else run_ours(args, rank, world, device)
 
     total_ms, e2e_s = slowest_replica(r["total_ms"], r["e2e_s"], world, device)
     ms_step = total_ms / args.steps
@@ -481,10 +644,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        spent, done, n = time_oracle(levels, args.batch, 12.0)
-        cpu = {"value": round(done / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first {n} GEMVs of the workload in step order ({done / 1e6:.0f} MB of weights, "
-                         f"{spent:.1f} s), plain C oracle, one thread"}
+        if args.workload.startswith("dequant_"):
+            cpu = dequant_cpu_baseline(args.workload)
+        else:
+            cpu = cpu_baselines(levels, args.batch)
 
     if rank == 0:
         line = {
@@ -495,6 +658,8 @@ def main():
             "config": {"workload": wname, "batch": args.batch,
                        "step_bytes": abytes,
                        "l2": ("inputs larger than L2 (weights per step exceed 129 MB)" if args.workload == "step"
+                              else "inputs larger than L2 (blocks in + fp32 out exceed 129 MB)"
+                              if args.workload in DEQUANT_TYPES
                               else "weights rotate over copies totalling at least 4x the 129 MB L2; "
                                    f"timed steps replay CUDA graphs of the qdq_gemv calls, {GROUP} steps "
                                    "(weight copies) per graph"),
@@ -503,6 +668,7 @@ def main():
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic, "peak_source": peaks["source"],
                          "kernel": ("stream1_kernel (persistent plan launch)" if args.workload == "step"
+                                    else "dequant_kernel" if args.workload in DEQUANT_TYPES
                                     else "mma_gemv_kernel + xsplit_kernel (tensor cores)"
                                     if args.batch >= mma_min_batch(levels[0][0].qtype)
                                     else "stream1_kernel (one GEMV per launch)")},
