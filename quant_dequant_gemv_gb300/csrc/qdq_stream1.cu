@@ -12,24 +12,27 @@
 // split across the consumer warps:
 //  * Tiles. A whole-row tile holds up to 64 complete rows; rows too long for
 //    eight per tile, or whose x does not fit the x window, are cut into
-//    2048-column chunks of up to 32 rows. Consumer warp w owns the 256-column
-//    slices w, w + 8, ... (one Q4_K / Q6_K super-block, eight q8_0 / q4_0 blocks)
-//    for every row of the tile; lane 4 r + c covers rows r and r + 8 and quarter
-//    c of a slice, 64 weights per row, in passes of 16 rows. Every warp works on
-//    every row, so even a level with a dozen rows per CTA keeps all eight warps
-//    busy.
-//  * x. At batch width 1 each warp stages its own x slices (plain and/or
-//    pre-scaled copies, plus the Q4_K sub-block sums) into a private area and
-//    holds a slice in registers across the passes of a tile. At widths 2-8 the
-//    warps stage one CTA-wide buffer with every batch column, and each decoded
-//    weight meets every column before the next is decoded.
+//    2048-column chunks of up to 32 rows. Work is split by 256-column slices
+//    (one Q4_K / Q6_K super-block, eight q8_0 / q4_0 blocks): lane 4 r + c
+//    covers row r (and r + 8) and quarter c of a slice, 64 weights per row.
+//    At batch width 1 fifteen consumer warps take the tile's (row pass, slice)
+//    units in turn, with passes of 8 or 16 rows, so a level with a dozen rows
+//    per CTA still gives every warp a unit. At widths 2-8 eight consumer warps
+//    each own the slices w, w + 8, ... of every row.
+//  * x. The consumer warps stage the window's x (plain and/or pre-scaled
+//    copies, every batch column) into one CTA-wide buffer and read it inside
+//    the word loop; the loads of a warp touch at most four 16-byte units each,
+//    which shared memory serves as broadcasts.
 //  * Partials. A warp keeps its row partials for the whole level in a
 //    shared-memory buffer (the chunks of a row add up in place); at the end of
 //    the level (or when the buffer is full) the consumer warps meet once, add
-//    the eight partials of each row in warp order and store y.
+//    the warps' partials of each row in warp order and store y.
 //  * Warp 0 streams tiles HBM -> shared memory with 1-D bulk copies into a byte
 //    ring and fetches ahead across level boundaries (W does not depend on x).
-//    Warp 1 owns the level dependency: one device-wide counter per level.
+//    The consumers own the level dependency: one device-wide counter per level,
+//    raised by one consumer thread after the level's y stores and polled by it
+//    before the next level's x is read (the other consumer warps wait at a
+//    named barrier).
 //  * Every wait is bounded (qdq_device.cuh).
 #include <cstdio>
 #include <type_traits>
@@ -42,8 +45,8 @@ static __device__ int s_status_s1;
 
 // Phase timestamps for performance analysis, compiled in only with -DQDQ_TRACE:
 // trace[(cta * nlevels + level) * 32 + slot] = %globaltimer (S1_TR) or the SM's
-// clock64 (S1_TRC, per-tile phases of the first consumer warp). Slots: 0-2 control
-// warp, 4-7 consumer level phases, 8-28 per tile (before the full wait, after it,
+// clock64 (S1_TRC, per-tile phases of the first consumer warp). Slots: 1-2 level
+// dependency wait, 3 units done, 4-7 consumer level phases, 8-28 per tile (before the full wait, after it,
 // after processing), 29 producer reaches the level's first tile, 30-31 producer
 // has issued the level's first and second tile.
 #ifdef QDQ_TRACE
@@ -66,26 +69,32 @@ static __device__ int s_status_s1;
 
 namespace s1 {
 
-constexpr int kCW = 8;                            // consumer warps
-constexpr int kFirstCW = 2;                       // warp 0 producer, warp 1 control
-constexpr int kThreads = 32 * (kCW + kFirstCW);
-constexpr int kPassRows = 16;                     // rows of one pass (lanes cover r and r + 8)
-constexpr int kTileRows = 64;                     // rows of a whole-row tile (up to four passes)
+constexpr int kFirstCW = 1;                       // warp 0 producer, then the consumers
+constexpr int kTileRows = 64;                     // rows of a whole-row tile
 constexpr int kChunkRows = 32;                    // rows of a chunked tile
-constexpr int kChunk = 2048;                      // columns of a chunk: kCW slices of kSlice
+constexpr int kChunk = 2048;                      // columns of a chunk: kSlicesPerChunk slices of kSlice
 constexpr int kSlice = 256;
+constexpr int kSlicesPerChunk = kChunk / kSlice;
 constexpr int kSlots = 8;                         // full/empty barrier pairs (tiles in the ring)
 constexpr int kFlushBar = 1;                      // named barrier of the consumer warps
-constexpr int kPartFloats = 4096;                 // level partial buffer: [warp][row][batch column]
+constexpr int kDepBar = 2;                        // the consumer warps wait here for a level dependency
+constexpr int kPartFloats = 6144;                 // level partial buffer: [warp][row][batch column]
 
-// Per batch width BT (1, 2, 4, 8). Batch 1 keeps x in registers, staged per warp;
-// wider batches read x from one CTA-wide buffer holding every batch column.
+// Per batch width BT (1, 2, 4, 8). x for every batch column of the staged window
+// sits in one CTA-wide buffer and is read inside the word loop. Batch 1 runs
+// fifteen consumer warps that take (row pass, slice) work units in turn; wider
+// batches run eight, warp w owning slices w, w + 8, ... of every tile.
 template <int BT>
 struct Cfg {
-    static constexpr int kRingBytes = BT == 1 ? 172032 : 114688;  // W ring: tiles packed in order
-    static constexpr int kMaxTileBytes = kRingBytes / 2;          // at least two tiles in flight
-    static constexpr int kXFloats = BT == 1 ? kCW * 1024 : 20480;  // x staging (per warp: 1024 at BT 1)
-    static constexpr int kBufRows = kPartFloats / (kCW * BT);      // rows of the level partial buffer
+    // consumer warps; at batch 1 the producer and fifteen consumers make sixteen
+    // warps, four per scheduler, whose registers (up to 128 each) fill the file
+    static constexpr int kCW = BT == 1 ? 15 : 8;
+    static constexpr int kThreads = 32 * (kCW + kFirstCW);
+    static constexpr int kRingBytes = BT == 1 ? 153600 : 114688;   // W ring: tiles packed in order
+    static constexpr int kMaxTileBytes = kRingBytes / 2;           // at least two tiles in flight
+    static constexpr int kXFloats = BT == 1 ? 10240 : 20480;       // x staging (CTA-wide)
+    // rows of the level partial buffer (a multiple of 8 keeps every later region aligned)
+    static constexpr int kBufRows = (kPartFloats / (kCW * BT)) & ~7;
     static constexpr int kNR = BT <= 4 ? 2 : 1;                    // rows per lane in one pass (BT > 1)
 };
 
@@ -101,12 +110,23 @@ struct Smem {
     static constexpr int kBars = kRing + 2 * kSlots * 4;
     static constexpr int kBytes = kBars + (2 * kSlots + 2) * 8;
 };
+template <int BT, int MAXD>
+constexpr bool smem_aligned() {
+    using S = Smem<BT, MAXD>;
+    return S::kX % 16 == 0 && S::kPart % 16 == 0 && S::kDst % 8 == 0 && S::kRanges % 8 == 0 && S::kRing % 4 == 0 &&
+           S::kBars % 8 == 0;
+}
+static_assert(smem_aligned<1, kMaxPlanDescs>() && smem_aligned<1, kMaxGroupDescs>() &&
+                  smem_aligned<2, kMaxPlanDescs>() && smem_aligned<2, kMaxGroupDescs>() &&
+                  smem_aligned<4, kMaxPlanDescs>() && smem_aligned<4, kMaxGroupDescs>() &&
+                  smem_aligned<8, kMaxPlanDescs>() && smem_aligned<8, kMaxGroupDescs>(),
+              "every shared-memory region at its access alignment (float4 x, int64 ranges, mbarriers)");
 static_assert(Smem<1, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
 static_assert(Smem<2, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
 static_assert(Smem<8, kMaxPlanDescs>::kBytes <= 227 * 1024, "shared memory budget");
 
 // ---------------------------------------------------------------------------
-// Tiles: identical sequence for the producer, the control warp and consumers.
+// Tiles: identical sequence for the producer and the consumers.
 // A whole-row tile holds up to 64 complete rows and every chunk of their x. It
 // is one contiguous bulk copy, except for rows whose length is a multiple of 128
 // bytes read with 32-bit loads: those are copied row by row to a pitch 16 bytes
@@ -130,26 +150,22 @@ struct Tile {
 };
 
 QDQ_DEV int nkinds(int kinds) { return __popc(kinds & 7); }
-// x floats staged per chunk. Batch 1, per warp: one 256-float slice per copy kind
-// plus eight Q4_K sub-block sums. Wider batches, CTA-wide: the chunk's 2048 columns
-// of every batch column in every kind, plus eight sums per slice and column.
+// x floats staged per chunk (CTA-wide): the chunk's 2048 columns of every batch
+// column in every kind.
 template <int BT>
 QDQ_DEV int xfloats_per_chunk(int kinds) {
-    if constexpr (BT == 1) return kSlice * nkinds(kinds) + ((kinds & 2) ? 8 : 0);
-    else return (kChunk * nkinds(kinds) + kCW * 8) * BT;
+    return kChunk * nkinds(kinds) * BT;
 }
 template <int BT>
 QDQ_DEV int window_chunks(int kinds) {
-    const int cap = BT == 1 ? Cfg<1>::kXFloats / kCW : Cfg<BT>::kXFloats;
-    const int w = cap / xfloats_per_chunk<BT>(kinds);
+    const int w = Cfg<BT>::kXFloats / xfloats_per_chunk<BT>(kinds);
     return w < 1 ? 1 : w;
 }
 // The kinds staged for a GEMV: every kind its level reads from this x when one
 // chunk of them fits, else only its own (the level's GEMVs then stage in turn).
 template <int BT>
 QDQ_DEV int staged_kinds(const DevDesc &d) {
-    const int cap = BT == 1 ? Cfg<1>::kXFloats / kCW : Cfg<BT>::kXFloats;
-    return xfloats_per_chunk<BT>(d.kinds) <= cap ? d.kinds : 1 << x_kind(d.type);
+    return xfloats_per_chunk<BT>(d.kinds) <= Cfg<BT>::kXFloats ? d.kinds : 1 << x_kind(d.type);
 }
 // Bytes of one row segment of a chunk, and the stage pitch of such segments.
 QDQ_DEV int seg_bytes(const DevDesc &d, int ccols) { return (ccols / blk_weights(d.type)) * blk_bytes(d.type); }
@@ -340,102 +356,25 @@ QDQ_DEV uint32_t tile_copy(const DevDesc &d, const Tile &t, uint32_t stage, uint
 }
 
 // ---------------------------------------------------------------------------
-// x slices in a warp's area. A slice is 256 floats in 64 16-byte units; unit
-// u = 16 q + i (lane quarter q reads units 16 q .. 16 q + 15) is stored at
-// 16 q + (i ^ 2 q), so the four quarters of a warp read four bank groups.
+// x in shared memory. A 256-float slice is 64 16-byte units; unit u = 16 q + i
+// (lane quarter q reads units 16 q .. 16 q + 15) is stored at 16 q + (i ^ 2 q),
+// so the four quarters of a warp read four bank groups.
 // ---------------------------------------------------------------------------
 QDQ_DEV int xunit(int u) { return (u & ~15) | ((u & 15) ^ ((u >> 3) & 6)); }
 
-// Stages x[col0 .. col0 + 2048 * (w1 - w0)) for warp w: slices of chunks w0..w1-1
-// in every copy kind, and the sub-block sums when Q4_K reads this x.
-QDQ_DEV void stage_x(const DevDesc &d, int kinds, int w0, int w1, int w, int lane, float *area) {
-    const int nk = nkinds(kinds);
-    const int sums_off = (w1 - w0) * kSlice * nk;
-    constexpr int kMaxWin = Cfg<1>::kXFloats / kCW / kSlice;  // chunks of one kind in a warp area
-    float4 v[2 * kMaxWin];
-#pragma unroll
-    for (int j = 0; j < kMaxWin; ++j) {
-        const int col = (w0 + j) * kChunk + w * kSlice + 8 * lane;
-        const bool ok = (w0 + j) < w1 && col < d.cols;
-        v[2 * j] = ok ? __ldcg((const float4 *)(d.x + col)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[2 * j + 1] = ok ? __ldcg((const float4 *)(d.x + col + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
-#pragma unroll
-    for (int j = 0; j < kMaxWin; ++j) {
-        if (w0 + j >= w1) break;
-        float *base = area + j * kSlice * nk;
-        int slot = 0;
-        if (kinds & 1) {  // plain
-            ((float4 *)(base + slot * kSlice))[u0] = v[2 * j];
-            ((float4 *)(base + slot * kSlice))[u1] = v[2 * j + 1];
-            ++slot;
-        }
-        if (kinds & 2) {  // Q4_K: columns 0..31 of each 64 meet low nibbles
-            const bool hi = (lane & 7) >= 4;
-            const float4 a = v[2 * j], b = v[2 * j + 1];
-            ((float4 *)(base + slot * kSlice))[u0] =
-                make_float4(a.x * nibble_scale(hi, 0), a.y * nibble_scale(hi, 1), a.z * nibble_scale(hi, 2),
-                            a.w * nibble_scale(hi, 3));
-            ((float4 *)(base + slot * kSlice))[u1] =
-                make_float4(b.x * nibble_scale(hi, 0), b.y * nibble_scale(hi, 1), b.z * nibble_scale(hi, 2),
-                            b.w * nibble_scale(hi, 3));
-            ++slot;
-            float s = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            if ((lane & 3) == 0) area[sums_off + 8 * j + (lane >> 2)] = s;
-        }
-        if (kinds & 4) {  // q4_0: columns 0..15 of each 32 meet low nibbles
-            const bool hi = (lane & 3) >= 2;
-            const float4 a = v[2 * j], b = v[2 * j + 1];
-            ((float4 *)(base + slot * kSlice))[u0] =
-                make_float4(a.x * nibble_scale(hi, 0), a.y * nibble_scale(hi, 1), a.z * nibble_scale(hi, 2),
-                            a.w * nibble_scale(hi, 3));
-            ((float4 *)(base + slot * kSlice))[u1] =
-                make_float4(b.x * nibble_scale(hi, 0), b.y * nibble_scale(hi, 1), b.z * nibble_scale(hi, 2),
-                            b.w * nibble_scale(hi, 3));
-        }
-    }
-    __syncwarp();
-}
-
-// The lane's 64 x values for its quarter c of the slice, as the units expect them:
-// consecutive columns 64 c .. 64 c + 63 (Q4_K, q8_0, q4_0), or for Q6_K the four
-// 16-column runs 128 h + 32 k + 16 m + (0..15), k = 0..3, with c = 2 h + m.
-QDQ_DEV void load_xr(const float *slice, int type, int c, XSlice &xr) {
-    const float4 *s4 = (const float4 *)slice;
-    if (type == QDQ_Q6_K) {
-        const int h = c >> 1, m = c & 1;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 v = s4[xunit(32 * h + 8 * k + 4 * m + i)];
-                xr.v[8 * k + 2 * i] = bits2(__float_as_uint(v.x), __float_as_uint(v.y));
-                xr.v[8 * k + 2 * i + 1] = bits2(__float_as_uint(v.z), __float_as_uint(v.w));
-            }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float4 v = s4[xunit(16 * c + i)];
-            xr.v[2 * i] = bits2(__float_as_uint(v.x), __float_as_uint(v.y));
-            xr.v[2 * i + 1] = bits2(__float_as_uint(v.z), __float_as_uint(v.w));
-        }
-    }
-}
-
 // ---------------------------------------------------------------------------
-// Batch columns 2..8 (BT > 1). x for every batch column sits in one CTA-wide
-// buffer: per chunk of the window (stride xfloats_per_chunk<BT>), kind slot k,
-// column b and slice w at (k * BT + b) * 2048 + w * 256 (swizzled units), and the
-// eight Q4_K sub-block sums of (b, w) at nk * BT * 2048 + (b * 8 + w) * 8.
+// x for every batch column sits in one CTA-wide buffer: per chunk of the window
+// (stride xfloats_per_chunk<BT>), kind slot k, column b and slice w at
+// (k * BT + b) * 2048 + w * 256 (swizzled units). The consumer warps stage
+// (chunk, slice) pairs in turn: warp cw takes pairs cw, cw + ncw, ...
 // ---------------------------------------------------------------------------
 template <int BT>
-QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, int w, int lane, float *xbuf) {
+QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, int cw, int ncw, int lane,
+                      float *xbuf) {
     const int nk = nkinds(kinds), stride = xfloats_per_chunk<BT>(kinds);
     const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
-    for (int j = 0; w0 + j < w1; ++j) {
+    for (int i = cw; i < (w1 - w0) * kSlicesPerChunk; i += ncw) {
+        const int j = i / kSlicesPerChunk, w = i % kSlicesPerChunk;
         float *chunk = xbuf + j * stride;
         const int col = (w0 + j) * kChunk + w * kSlice + 8 * lane;
 #pragma unroll
@@ -450,19 +389,6 @@ QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, in
                 sl[u0] = a;
                 sl[u1] = c;
                 ++slot;
-            }
-            if (kinds & 2) {  // Q4_K: columns 0..31 of each 64 meet low nibbles
-                const bool hi = (lane & 7) >= 4;
-                float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
-                sl[u0] = make_float4(a.x * nibble_scale(hi, 0), a.y * nibble_scale(hi, 1), a.z * nibble_scale(hi, 2),
-                                     a.w * nibble_scale(hi, 3));
-                sl[u1] = make_float4(c.x * nibble_scale(hi, 0), c.y * nibble_scale(hi, 1), c.z * nibble_scale(hi, 2),
-                                     c.w * nibble_scale(hi, 3));
-                ++slot;
-                float sm = ((a.x + a.y) + (a.z + a.w)) + ((c.x + c.y) + (c.z + c.w));
-                sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-                sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-                if ((lane & 3) == 0) chunk[nk * BT * kChunk + (b * 8 + w) * 8 + (lane >> 2)] = sm;
             }
             if (kinds & 4) {  // q4_0: columns 0..15 of each 32 meet low nibbles
                 const bool hi = (lane & 3) >= 2;
@@ -483,10 +409,17 @@ QDQ_DEV void xpairs_b(const float *xs, int b, int u, uint64_t &p0, uint64_t &p1)
     p1 = bits2(__float_as_uint(v.z), __float_as_uint(v.w));
 }
 
-// Q4_K, NR rows x BT columns: each word is decoded once and meets every column.
-// Sub-blocks are recentred as in unit_q4k (q4k_center).
+// Q4_K, NR rows x BT columns: each word is decoded once, into exact weights, and
+// every weight meets every column. Lane quarter c covers chunk c of the
+// super-block: sub-block 2c in the low nibbles (columns 64c .. 64c+31) and 2c+1 in
+// the high nibbles (64c+32 ..). A nibble left at bit position p reads as the float
+// 2^23 + q 2^p; one fma with (2^-p, -2^(23-p)) gives q exactly, and a second,
+// q * (d sc) - dmin mn, gives the weight with the single rounding of the format's
+// formula (d sc q is exact in fp32: an 11-bit fp16 significand times a 6-bit
+// scale times a 4-bit quant). So each weight is the oracle's, and the dot product
+// has no factored terms that could cancel.
 template <int NR, int BT>
-QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const float *sums, float (&out)[NR][BT]) {
+QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, float (&out)[NR][BT]) {
     uint4 H[NR], Qa[NR], Qb[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -494,37 +427,39 @@ QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const 
         Qa[r] = ld4(wrow[r] + 16 + 32 * c);
         Qb[r] = ld4(wrow[r] + 32 + 32 * c);
     }
-    float s_lo[NR], s_hi[NR], m_lo[NR], m_hi[NR];
-    uint64_t C_a[NR], C_b[NR], C_h[NR];
+    // q from nibbles at positions (0, 8), (16, 8) [low] and (4, 12) [high]
+    const uint64_t P08 = pack2(1.0f, 0.00390625f), N08 = pack2(-kTwo23, -32768.0f);
+    const uint64_t P168 = pack2(1.52587890625e-05f, 0.00390625f), N168 = pack2(-128.0f, -32768.0f);
+    const uint64_t P412 = pack2(0.0625f, 0.000244140625f), N412 = pack2(-524288.0f, -2048.0f);
+    uint64_t DL[NR], ML[NR], DH[NR], MH[NR];
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
         uint32_t sc2, mn2;
         q4k_pair_fields(H[r].y, H[r].z, H[r].w, c, &sc2, &mn2);
         const float d = half_bits_to_float(H[r].x & 0xFFFF), dmin = half_bits_to_float(H[r].x >> 16);
-        s_lo[r] = d * (float)(sc2 & 0xFF);
-        s_hi[r] = d * (float)(sc2 >> 8);
-        const float r_lo = q4k_center(s_lo[r], dmin * (float)(mn2 & 0xFF), &m_lo[r]);
-        const float r_hi = q4k_center(s_hi[r], dmin * (float)(mn2 >> 8), &m_hi[r]);
-        C_a[r] = pack2(fmaf(r_lo, 1.0f, kTwo23), fmaf(r_lo, 256.0f, kTwo23));
-        C_b[r] = pack2(fmaf(r_lo, 65536.0f, kTwo23), fmaf(r_lo, 256.0f, kTwo23));
-        C_h[r] = pack2(fmaf(r_hi, 16.0f, kTwo23), fmaf(r_hi, 4096.0f, kTwo23));
+        const float s_lo = d * (float)(sc2 & 0xFF), s_hi = d * (float)(sc2 >> 8);
+        const float m_lo = -(dmin * (float)(mn2 & 0xFF)), m_hi = -(dmin * (float)(mn2 >> 8));
+        DL[r] = pack2(s_lo, s_lo);
+        ML[r] = pack2(m_lo, m_lo);
+        DH[r] = pack2(s_hi, s_hi);
+        MH[r] = pack2(m_hi, m_hi);
     }
-    uint64_t lo[NR][BT], hi[NR][BT];
+    uint64_t acc[NR][BT], acc2[NR][BT];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int b = 0; b < BT; ++b) lo[r][b] = hi[r][b] = 0;
+        for (int b = 0; b < BT; ++b) acc[r][b] = acc2[r][b] = 0;
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
-        uint64_t q0[NR], q1[NR], q2[NR], q3[NR];
+        uint64_t w0[NR], w1[NR], w2[NR], w3[NR];
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
             const uint32_t w[8] = {Qa[r].x, Qa[r].y, Qa[r].z, Qa[r].w, Qb[r].x, Qb[r].y, Qb[r].z, Qb[r].w};
             const uint32_t v = w[t], u = v >> 16;
-            q0[r] = fsub2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), C_a[r]);
-            q1[r] = fsub2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), C_b[r]);
-            q2[r] = fsub2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), C_h[r]);
-            q3[r] = fsub2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), C_h[r]);
+            w0[r] = ffma2(ffma2(bits2(mask_magic<0xFu>(v), mask_magic<0xF00u>(v)), P08, N08), DL[r], ML[r]);
+            w1[r] = ffma2(ffma2(bits2(mask_magic<0xF0000u>(v), mask_magic<0xF00u>(u)), P168, N168), DL[r], ML[r]);
+            w2[r] = ffma2(ffma2(bits2(mask_magic<0xF0u>(v), mask_magic<0xF000u>(v)), P412, N412), DH[r], MH[r]);
+            w3[r] = ffma2(ffma2(bits2(mask_magic<0xF0u>(u), mask_magic<0xF000u>(u)), P412, N412), DH[r], MH[r]);
         }
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
@@ -533,20 +468,16 @@ QDQ_DEV void dotb_q4k(const uint8_t *const *wrow, int c, const float *xs, const 
             xpairs_b(xs, b, 16 * c + 8 + t, xh0, xh1);
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                lo[r][b] = ffma2(q1[r], xl1, ffma2(q0[r], xl0, lo[r][b]));
-                hi[r][b] = ffma2(q3[r], xh1, ffma2(q2[r], xh0, hi[r][b]));
+                acc[r][b] = ffma2(w1[r], xl1, ffma2(w0[r], xl0, acc[r][b]));
+                acc2[r][b] = ffma2(w3[r], xh1, ffma2(w2[r], xh0, acc2[r][b]));
             }
         }
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
+    for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int b = 0; b < BT; ++b) {
-            const float l = lo_of(lo[r][b]) + hi_of(lo[r][b]), h = lo_of(hi[r][b]) + hi_of(hi[r][b]);
-            out[r][b] = (s_lo[r] * l + s_hi[r] * h) -
-                        (m_lo[r] * sums[b * 64 + 2 * c] + m_hi[r] * sums[b * 64 + 2 * c + 1]);
-        }
-    }
+        for (int b = 0; b < BT; ++b)
+            out[r][b] = (lo_of(acc[r][b]) + hi_of(acc[r][b])) + (lo_of(acc2[r][b]) + hi_of(acc2[r][b]));
 }
 
 // Q6_K, c = 2 h + m (see dot_q6k), NR rows x BT columns.
@@ -739,85 +670,12 @@ QDQ_DEV const uint8_t *row_ptr(const uint8_t *stage_p, const RowGeo &g, int r) {
     return stage_p + (uint32_t)(r * g.pitch) + ((g.src_lo + (uint32_t)(r * g.rb)) & 15u);
 }
 
-// This warp's slices of a tile, for one format: 256-column slices cw, cw + 8, ...
-// of whole rows, or slice cw of a chunk. For each slice the x registers are
-// loaded once and serve every pass of up to 16 rows; the warp's row partials go
-// to its own column of the level buffer (stored for the first contribution,
-// added otherwise).
-template <int TYPE>
-QDQ_DEV void tile_slices(const Tile &tl, const DevDesc &d, const uint8_t *stage_p, const RowGeo &geo,
-                         const float *area, int cw, int r8, int c, float *mycol) {
-    constexpr int QK = (TYPE == QDQ_Q4_K || TYPE == QDQ_Q6_K) ? 256 : 32;
-    constexpr int SB = (kSlice / QK) * blk_bytes(TYPE);  // slice bytes
-    constexpr int KIND = x_kind(TYPE);
-    const int nk = nkinds(tl.skinds);
-    const int slot = __popc(tl.skinds & ((1 << KIND) - 1));
-    const int nslices = (tl.ccols + kSlice - 1) / kSlice;
-    const int k0 = tl.whole ? cw : 8 * tl.chunk + cw;
-    const int kend = tl.whole ? nslices : (cw < nslices ? k0 + 1 : k0);
-    const int npass = (tl.nrows + kPassRows - 1) / kPassRows;
-    bool fresh = tl.first;
-    for (int k = k0; k < kend; k += kCW) {
-        const int jw = (k >> 3) - tl.xw0;  // chunk of the slice in the x window
-        XSlice xr;
-        load_xr(area + jw * kSlice * nk + slot * kSlice, TYPE, c, xr);
-        if constexpr (TYPE == QDQ_Q4_K) {
-            const float *sums = area + tl.xwn * kSlice * nk + 8 * jw;
-            xr.s0 = sums[2 * c];
-            xr.s1 = sums[2 * c + 1];
-        }
-        const int kcols = d.cols - k * kSlice;
-        const int nb = (kcols < kSlice ? kcols : kSlice) / QK;
-        const uint32_t koff = (uint32_t)(tl.whole ? k : cw) * SB;
-        for (int p = 0; p < npass; ++p) {
-            const int rp = p * kPassRows, left = tl.nrows - rp;
-            float o0 = 0.f, o1 = 0.f;
-            if (left > 8) {
-                const int rb = r8 + 8 < left ? rp + r8 + 8 : tl.nrows - 1;
-                const uint8_t *wrow[2] = {row_ptr(stage_p, geo, rp + r8) + koff, row_ptr(stage_p, geo, rb) + koff};
-                float acc[2] = {0.f, 0.f};
-                if constexpr (TYPE == QDQ_Q4_K) unit_q4k<2>(wrow, c, xr, acc);
-                else if constexpr (TYPE == QDQ_Q6_K) unit_q6k<2>(wrow, c, xr, acc);
-                else if (2 * c < nb) {
-                    if constexpr (TYPE == QDQ_Q8_0) unit_q8_0<2>(wrow, c, nb, xr, acc);
-                    else unit_q4_0<2>(wrow, c, nb, xr, acc);
-                }
-                o0 = acc[0];
-                o1 = acc[1];
-            } else {
-                const int ra = r8 < left ? rp + r8 : tl.nrows - 1;
-                const uint8_t *wrow[1] = {row_ptr(stage_p, geo, ra) + koff};
-                float acc[1] = {0.f};
-                if constexpr (TYPE == QDQ_Q4_K) unit_q4k<1>(wrow, c, xr, acc);
-                else if constexpr (TYPE == QDQ_Q6_K) unit_q6k<1>(wrow, c, xr, acc);
-                else if (2 * c < nb) {
-                    if constexpr (TYPE == QDQ_Q8_0) unit_q8_0<1>(wrow, c, nb, xr, acc);
-                    else unit_q4_0<1>(wrow, c, nb, xr, acc);
-                }
-                o0 = acc[0];
-            }
-            o0 += __shfl_xor_sync(0xffffffffu, o0, 1);
-            o1 += __shfl_xor_sync(0xffffffffu, o1, 1);
-            o0 += __shfl_xor_sync(0xffffffffu, o0, 2);
-            o1 += __shfl_xor_sync(0xffffffffu, o1, 2);
-            if (c == 0) {
-                float *q = mycol + rp + r8;
-                if (r8 < left) q[0] = fresh ? o0 : q[0] + o0;
-                if (r8 + 8 < left) q[8] = fresh ? o1 : q[8] + o1;
-            }
-        }
-        fresh = false;
-    }
-    if (fresh && c == 0)  // no slice of this warp in the tile: zero partials
-        for (int rr = r8; rr < tl.nrows; rr += 8) mycol[rr] = 0.f;
-}
-
-// Batch columns 2..8: rows r, r + 8, ... (NR; lane 4 r + c) of one slice against
-// every column; the row partials go to this warp's column of the level buffer as
+// Rows r, r + 8, ... (NR; lane 4 r + c) of one slice against every batch
+// column; the row partials go to this warp's column of the level buffer as
 // [row][batch column].
 template <int TYPE, int NR, int BT>
 QDQ_DEV void pass_rows_b(const uint8_t *stage_p, const RowGeo &geo, uint32_t koff, int rp, int left, int r8, int c,
-                         int nb, const float *xs, const float *sums, bool fresh, float *mycol) {
+                         int nb, const float *xs, bool fresh, float *mycol) {
     const uint8_t *wrow[NR];
 #pragma unroll
     for (int i = 0; i < NR; ++i) {
@@ -825,7 +683,7 @@ QDQ_DEV void pass_rows_b(const uint8_t *stage_p, const RowGeo &geo, uint32_t kof
         wrow[i] = row_ptr(stage_p, geo, rp + (r < left ? r : left - 1)) + koff;
     }
     float acc[NR][BT];
-    if constexpr (TYPE == QDQ_Q4_K) dotb_q4k<NR, BT>(wrow, c, xs, sums, acc);
+    if constexpr (TYPE == QDQ_Q4_K) dotb_q4k<NR, BT>(wrow, c, xs, acc);
     else if constexpr (TYPE == QDQ_Q6_K) dotb_q6k<NR, BT>(wrow, c, xs, acc);
     else if constexpr (TYPE == QDQ_Q8_0) dotb_q8_0<NR, BT>(wrow, c, nb, xs, acc);
     else dotb_q4_0<NR, BT>(wrow, c, nb, xs, acc);
@@ -864,18 +722,17 @@ QDQ_DEV void tile_slices_b(const Tile &tl, const DevDesc &d, const uint8_t *stag
     const int kend = tl.whole ? nslices : (cw < nslices ? k0 + 1 : k0);
     const int n = tl.nrows;
     bool fresh = tl.first;
-    for (int k = k0; k < kend; k += kCW) {
+    for (int k = k0; k < kend; k += Cfg<BT>::kCW) {
         const float *chunk = xbuf + ((k >> 3) - tl.xw0) * stride;
         const float *xs = chunk + slot * BT * kChunk + (k & 7) * kSlice;
-        const float *sums = chunk + nk * BT * kChunk + (k & 7) * 8;
         const int kcols = d.cols - k * kSlice;
         const int nb = (kcols < kSlice ? kcols : kSlice) / QK;
         const uint32_t koff = (uint32_t)(tl.whole ? k : cw) * SB;
         for (int rp = 0; rp < n; rp += 8 * NR) {
             if (NR == 2 && n - rp > 8)
-                pass_rows_b<TYPE, NR, BT>(stage_p, geo, koff, rp, n - rp, r8, c, nb, xs, sums, fresh, mycol);
+                pass_rows_b<TYPE, NR, BT>(stage_p, geo, koff, rp, n - rp, r8, c, nb, xs, fresh, mycol);
             else
-                pass_rows_b<TYPE, 1, BT>(stage_p, geo, koff, rp, n - rp, r8, c, nb, xs, sums, fresh, mycol);
+                pass_rows_b<TYPE, 1, BT>(stage_p, geo, koff, rp, n - rp, r8, c, nb, xs, fresh, mycol);
         }
         fresh = false;
     }
@@ -885,24 +742,74 @@ QDQ_DEV void tile_slices_b(const Tile &tl, const DevDesc &d, const uint8_t *stag
             for (int b = 0; b < BT; ++b) mycol[rr * BT + b] = 0.f;
 }
 
+// Batch 1: the tile's work units (row pass, slice) are dealt to the consumer warps
+// in turn. A pass covers 8 rows (one per lane group, NR = 1) or 16 (NR = 2, lanes
+// also take row r + 8), whichever finishes the tile in fewer unit rounds. A warp
+// adds its units' row partials into its own column of the level buffer, which
+// the tile's first chunk has zeroed.
+template <int TYPE, int NR>
+QDQ_DEV void tile_units1_nr(const Tile &tl, const DevDesc &d, const uint8_t *stage_p, const RowGeo &geo,
+                            const float *xbuf, int cw, int r8, int c, float *mycol, int nslices) {
+    constexpr int QK = (TYPE == QDQ_Q4_K || TYPE == QDQ_Q6_K) ? 256 : 32;
+    constexpr int SB = (kSlice / QK) * blk_bytes(TYPE);
+    constexpr int KIND = x_kind(TYPE);
+    constexpr int kCW = Cfg<1>::kCW;
+    const int nk = nkinds(tl.skinds);
+    const int slot = __popc(tl.skinds & ((1 << KIND) - 1));
+    const int stride = xfloats_per_chunk<1>(tl.skinds);
+    const int n = tl.nrows, rows_pp = 8 * NR;
+    const int npass = (n + rows_pp - 1) / rows_pp;
+    // unit u = p * nslices + kk, stepped by kCW without divisions in the loop
+    int p = cw / nslices, kk = cw - p * nslices;
+    const int dp = kCW / nslices, dk = kCW - dp * nslices;
+    for (; p < npass; p += dp, kk += dk) {
+        if (kk >= nslices) {
+            kk -= nslices;
+            ++p;
+            if (p >= npass) break;
+        }
+        const int k = tl.whole ? kk : kSlicesPerChunk * tl.chunk + kk;  // slice of the row
+        const float *chunk = xbuf + ((k >> 3) - tl.xw0) * stride;
+        const float *xs = chunk + slot * kChunk + (k & 7) * kSlice;
+        const int kcols = d.cols - k * kSlice;
+        const int nb = (kcols < kSlice ? kcols : kSlice) / QK;
+        const int rp = p * rows_pp;
+        pass_rows_b<TYPE, NR, 1>(stage_p, geo, (uint32_t)kk * SB, rp, n - rp, r8, c, nb, xs, false, mycol);
+    }
+}
+
+template <int TYPE>
+QDQ_DEV void tile_units1(const Tile &tl, const DevDesc &d, const uint8_t *stage_p, const RowGeo &geo,
+                         const float *xbuf, int cw, int r8, int c, float *mycol) {
+    constexpr int kCW = Cfg<1>::kCW;
+    const int nslices = (tl.ccols + kSlice - 1) / kSlice;
+    // rounds of units each warp runs; a unit of NR rows costs about NR + 1 row
+    // units (its fixed part: pointers, scales, the row reduction)
+    const int rounds1 = (((tl.nrows + 7) / 8) * nslices + kCW - 1) / kCW;
+    const int rounds2 = (((tl.nrows + 15) / 16) * nslices + kCW - 1) / kCW;
+    if (3 * rounds2 <= 2 * rounds1)
+        tile_units1_nr<TYPE, 2>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, nslices);
+    else
+        tile_units1_nr<TYPE, 1>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, nslices);
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int BT, int MAXD, int MAXL>
-__global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_constant__ StreamArgs<MAXD, MAXL> a) {
+__global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __grid_constant__ StreamArgs<MAXD, MAXL> a) {
     using SM = Smem<BT, MAXD>;
     constexpr int kBufRows = Cfg<BT>::kBufRows;
+    constexpr int kCW = Cfg<BT>::kCW;
+    constexpr int kThreads = Cfg<BT>::kThreads;
     extern __shared__ __align__(1024) uint8_t smem[];
-    float *xareas = (float *)(smem + SM::kX);  // batch 1: per-warp x areas; wider: one CTA-wide buffer
+    float *xbuf = (float *)(smem + SM::kX);  // x of the staged window, every batch column
     float *part = (float *)(smem + SM::kPart);
     uint64_t *dst = (uint64_t *)(smem + SM::kDst);
     int *dstride = (int *)(smem + SM::kDstStride);
     int64_t *ranges = (int64_t *)(smem + SM::kRanges);
     const uint32_t ring_a = smem_u32(smem);
     const uint32_t full_a = smem_u32(smem + SM::kBars), empty_a = full_a + 8 * kSlots;
-    // lvl: this CTA's consumers finished a level; dep: every CTA finished the
-    // previous level (arrival by the control warp).
-    const uint32_t lvl_a = empty_a + 8 * kSlots, dep_a = lvl_a + 8;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cta = blockIdx.x, P = gridDim.x;
@@ -914,8 +821,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
             mbar_init(full_a + 8 * s, 1);
             mbar_init(empty_a + 8 * s, kCW);
         }
-        mbar_init(lvl_a, kCW);
-        mbar_init(dep_a, 1);
         fence_mbar_init();
     }
     for (int L = 0; L < a.nlevels; ++L)
@@ -971,55 +876,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
         return;
     }
 
-    if (warp == 1) {
-        // ------------------------------------------------------------ control
-        // Publishes level L once this CTA's consumers have finished it, waits until
-        // every CTA has, and releases the consumers into level L+1. lvl completes
-        // one phase per level in which this CTA has tiles, and dep is arrived only
-        // for such levels; neither can run two phases ahead of its waiter.
-        if (!levels_synced) return;
-        auto has_tiles = [&](int L) {
-            for (int g = a.level_start[L]; g < a.level_start[L + 1]; ++g)
-                if (ranges[2 * g] < ranges[2 * g + 1]) return true;
-            return false;
-        };
-        int lvl_phase = 0;
-        bool prev_had = has_tiles(0);
-        for (int L = 1; L < a.nlevels; ++L) {
-            if (lane == 0) S1_TR(L, 0);
-            if (prev_had) mbar_wait_spin(lvl_a, (lvl_phase++) & 1, status);
-            if (lane == 0) {
-                S1_TR(L, 1);
-                // The consumers' y stores are ordered before their arrivals (CTA
-                // scope); the release makes them visible at GPU scope with the count.
-                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&a.counters[L - 1]) : "memory");
-                wait_counter(&a.counters[L - 1], (unsigned)P, status, kWaitLimitNs);
-                S1_TR(L, 2);
-            }
-            __syncwarp();
-            const bool had = has_tiles(L);
-            if (had && lane == 0) mbar_arrive(dep_a);
-            prev_had = had;
-        }
-        if (prev_had) mbar_wait_spin(lvl_a, (lvl_phase++) & 1, status);
-        if (lane == 0) {
-            __threadfence();
-            const unsigned old = atomicAdd(&a.counters[a.nlevels - 1], 1u);
-            if (old == (unsigned)P - 1) {  // every CTA has passed every wait: reset for the next run
-                for (int i = 0; i < a.nlevels; ++i) a.counters[i] = 0u;
-                __threadfence();
-            }
-        }
-        return;
-    }
-
     // ---------------------------------------------------------------- consumers
     const int cw = warp - kFirstCW;
     const int ctid = (int)threadIdx.x - 32 * kFirstCW;
     const int r8 = lane >> 2, c = lane & 3;
-    float *area = BT == 1 ? xareas + cw * (Cfg<1>::kXFloats / kCW) : xareas;
     float *mypart = part + cw * kBufRows * BT;
-    int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0, dep_phase = 0;
+    int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0;
     int buf_rows = 0, rg_base = 0;
     uint32_t ring_next = 0;
     bool had_tiles = false, dep_pending = false, level_staged = false;
@@ -1065,22 +927,24 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
         [&](const Tile &tl, int e, const DevDesc &d) {
             had_tiles = true;
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 4);
+            if (dep_pending) {  // wait until every CTA has released the previous level
+                if (cw == 0 && lane == 0) {
+                    S1_TR(cur_level, 1);
+                    wait_counter(&a.counters[cur_level - 1], (unsigned)P, status, kWaitLimitNs);
+                    S1_TR(cur_level, 2);
+                }
+                named_bar_sync(kDepBar, kCW * 32);
+                dep_pending = false;
+                cur_e = -1;  // x is read again after the dependency
+            }
             if (e != cur_e) {
-                if (dep_pending) {  // the previous level is complete on every CTA
-                    mbar_wait_spin(dep_a, (dep_phase++) & 1, status);
-                    dep_pending = false;
-                }
                 cur_e = e;
-                if constexpr (BT == 1) {
-                    stage_x(d, tl.skinds, tl.xw0, tl.xw0 + tl.xwn, cw, lane, area);
-                } else {
-                    // the buffer is shared: a later x of the same level waits for every
-                    // warp to be done with it; then every warp stages its slices
-                    if (level_staged) named_bar_sync(kFlushBar, kCW * 32);
-                    stage_xb<BT>(d, tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, lane, area);
-                    named_bar_sync(kFlushBar, kCW * 32);
-                    level_staged = true;
-                }
+                // the buffer is shared: a later x of the same level waits for every
+                // warp to be done with it; then every warp stages its slices
+                if (level_staged) named_bar_sync(kFlushBar, kCW * 32);
+                stage_xb<BT>(d, tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, xbuf);
+                named_bar_sync(kFlushBar, kCW * 32);
+                level_staged = true;
             }
             if (tl.first) {  // a new row group: its rows in the partial buffer
                 // Rows whose earlier columns sit in this buffer are stored first.
@@ -1091,6 +955,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                     for (int i = lane; i < tl.nrows; i += 32)
                         dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) | (tl.first_win ? 0u : 1u),
                         dstride[rg_base + i] = (int)d.rows;
+                if constexpr (BT == 1) {  // batch 1 adds every unit into the warp's column
+                    for (int i = lane; i < tl.nrows; i += 32) mypart[rg_base + i] = 0.f;
+                    __syncwarp();
+                }
             }
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 5);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 8 + 3 * tiles_in_level);
@@ -1115,17 +983,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
                 float *mycol = mypart + rg_base * BT;
                 if constexpr (BT == 1) {
                     switch (d.type) {
-                        case QDQ_Q4_K: tile_slices<QDQ_Q4_K>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                        case QDQ_Q6_K: tile_slices<QDQ_Q6_K>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                        case QDQ_Q8_0: tile_slices<QDQ_Q8_0>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                        default: tile_slices<QDQ_Q4_0>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        case QDQ_Q4_K: tile_units1<QDQ_Q4_K>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        case QDQ_Q6_K: tile_units1<QDQ_Q6_K>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        case QDQ_Q8_0: tile_units1<QDQ_Q8_0>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        default: tile_units1<QDQ_Q4_0>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
                     }
                 } else {
                     switch (d.type) {
-                        case QDQ_Q4_K: tile_slices_b<QDQ_Q4_K, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                        case QDQ_Q6_K: tile_slices_b<QDQ_Q6_K, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                        case QDQ_Q8_0: tile_slices_b<QDQ_Q8_0, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
-                        default: tile_slices_b<QDQ_Q4_0, BT>(tl, d, stage_p, geo, area, cw, r8, c, mycol); break;
+                        case QDQ_Q4_K: tile_slices_b<QDQ_Q4_K, BT>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        case QDQ_Q6_K: tile_slices_b<QDQ_Q6_K, BT>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        case QDQ_Q8_0: tile_slices_b<QDQ_Q8_0, BT>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        default: tile_slices_b<QDQ_Q4_0, BT>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
                     }
                 }
             }
@@ -1134,15 +1002,28 @@ __global__ void __launch_bounds__(kThreads, 1) stream1_kernel(const __grid_const
             if (lane == 0) mbar_arrive(empty_a + 8 * s);
             ++t;
         },
-        [&](int) {
-            if (buf_rows > 0) flush();
-            if (cw == 0 && lane == 0) S1_TR(cur_level, 7);
-            if (levels_synced && had_tiles) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(lvl_a);  // release (CTA scope) of the level's y stores
+        [&](int L) {
+            if (cw == 0 && lane == 0) S1_TR(cur_level, 3);
+            if (buf_rows > 0) flush();  // ends with a barrier of the consumer warps after their y stores
+            if (cw == 0 && lane == 0) {
+                S1_TR(cur_level, 7);
+                if (levels_synced) {
+                    if (L + 1 < a.nlevels) {
+                        // The barrier orders every consumer's y stores before this
+                        // release, which makes them visible at GPU scope with the count.
+                        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&a.counters[L]) : "memory");
+                    } else {
+                        __threadfence();
+                        const unsigned old = atomicAdd(&a.counters[L], 1u);
+                        if (old == (unsigned)P - 1) {  // every CTA has passed every wait: reset for the next run
+                            for (int i = 0; i < a.nlevels; ++i) a.counters[i] = 0u;
+                            __threadfence();
+                        }
+                    }
+                }
             }
             had_tiles = false;
-            dep_pending = false;  // a level without tiles here needs no release
+            dep_pending = false;  // a level without tiles here waits for nothing
         });
 }
 
@@ -1169,9 +1050,9 @@ static int launch1(const void *args, int grid, bool cooperative, cudaStream_t st
     void *params[] = {const_cast<void *>(args)};
     const cudaError_t e =
         cooperative
-            ? cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(s1::kThreads), params, (size_t)smem,
+            ? cudaLaunchCooperativeKernel((const void *)kern, dim3(grid), dim3(s1::Cfg<BT>::kThreads), params, (size_t)smem,
                                           stream)
-            : cudaLaunchKernel((const void *)kern, dim3(grid), dim3(s1::kThreads), params, (size_t)smem, stream);
+            : cudaLaunchKernel((const void *)kern, dim3(grid), dim3(s1::Cfg<BT>::kThreads), params, (size_t)smem, stream);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return QDQ_ERR_CUDA;
