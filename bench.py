@@ -217,7 +217,7 @@ def gemv_launches(g, batch):
     if batch < mma_min_batch(g.qtype):
         return 1
     per = 32 if g.qtype == synth.Q6_K else 64
-    return 2 * ((batch + per - 1) // per)  # split-x kernel + tensor-core kernel per batch slice
+    return (batch + per - 1) // per  # one tensor-core launch per batch slice
 
 
 def run_dequant(args, device):
@@ -669,7 +669,7 @@ def main():
                          "traffic": traffic, "peak_source": peaks["source"],
                          "kernel": ("stream1_kernel (persistent plan launch)" if args.workload == "step"
                                     else "dequant_kernel" if args.workload in DEQUANT_TYPES
-                                    else "mma_gemv_kernel + xsplit_kernel (tensor cores)"
+                                    else "mma_gemv_kernel (tensor cores)"
                                     if args.batch >= mma_min_batch(levels[0][0].qtype)
                                     else "stream1_kernel (one GEMV per launch)")},
             "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s",

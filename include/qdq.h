@@ -97,9 +97,8 @@ int qdq_dequant_async(int type, const void *blocks, int64_t n, float *out_f32,
  * CUDA-core kernel (each decoded weight meets every batch column); larger
  * batches the tensor-core path (exact integer quants x bf16-split x on tcgen05,
  * scales applied per group in fp32). Any row width is accepted (wide rows are
- * split into column chunks inside the streaming kernel). The tensor-core path takes scratch for
- * the split x (4 * batch * cols bytes, at most 64 batch columns at a time) from
- * a stream-ordered memory pool of the library's own.
+ * split into column chunks inside the streaming kernel). Neither path allocates
+ * memory: the tensor-core kernel splits x into its bf16 operand in shared memory.
  * ------------------------------------------------------------------------- */
 int qdq_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y,
              int batch, qdq_stream_t stream);

@@ -13,16 +13,18 @@
 // input. Z_g accumulates q x_hi + q x_lo in fp32 tensor memory (two MMAs with
 // N = b_pad), one accumulator region per group.
 //
-// X is split once per call by a small kernel into a scratch buffer already in
-// the MMA's canonical K-major layout (and, for Q4_K, the group sums X_g), so
-// every CTA copies its B tiles with one bulk copy per 64 columns.
+// Each CTA splits its own columns of X, sub-chunk by sub-chunk, into the
+// MMA's canonical K-major layout in shared memory (and, for Q4_K, the group sums
+// X_g), so a call needs no scratch memory and no second launch.
 //
 // One CTA per SM, 19 warps:
 //   warp 0      copies the raw blocks of 128 rows x 256 weights into a ring, with
 //               2-D tensor copies of W viewed as [rows / g][g row_bytes]
 //               (L2 evict-first);
 //   warp 1      owns the tensor memory; its elected lane issues the MMAs;
-//   warp 2      copies the split X of each 64-column sub-chunk into a ring;
+//   warp 2      reads the fp32 x of each 64-column sub-chunk, splits it into
+//               the X slot of the sub-chunk's A stage and (Q4_K) stores the
+//               sub-chunk's two group sums in a ring of its own;
 //   warps 3-18  turn quants into exact bf16 (a byte permute puts each quant under
 //               the bf16 exponent of 128, a bf16 subtraction removes the offset),
 //               store them to tensor memory and later read the group
@@ -105,8 +107,8 @@ __host__ __device__ constexpr int groups_per_sub(int type) { return type == QDQ_
 // Padded batches up to 32 decode in four groups of four warps, each group taking
 // every fourth sub-chunk whole (see the decode warps), when tensor memory holds
 // four accumulator sets: four sub-chunks are then in flight, each in its own set.
-// A group waits for its set's MMAs with mbarrier parity; with fewer sets than
-// groups a set could be two phases ahead of a waiter, which parity cannot tell.
+// The ring then has exactly four sets, so set G belongs to group G alone, and the
+// group's parity wait on it cannot confuse two phases.
 // Wider batches keep all sixteen warps on every sub-chunk (three sets suffice).
 __host__ __device__ constexpr bool rr_groups(int type, int bpad) {
     return bpad <= 32 && groups_per_sub(type) * bpad * 4 <= (int)(512 - 32 * 4);
@@ -118,8 +120,7 @@ __host__ __device__ constexpr bool stacked_b(int type, int bpad) {
 
 struct MmaArgs {
     const uint8_t *W;   // rows x row_bytes
-    const uint8_t *xs;  // split X: per K-step of 16 columns, 2 b_pad rows x 16 bf16 (64 b_pad bytes)
-    const float *xsum;  // Q4_K: sum of x over each 32-column group, [cols / 32][b_pad]
+    const float *x;     // this launch's batch slice of x, [batch][cols] fp32
     float *y;           // [batch][rows]
     int64_t rows, cols, row_bytes;
     int64_t rows_full;  // rows reached through the tensor map (a multiple of g)
@@ -137,15 +138,22 @@ struct MmaArgs {
 };
 
 struct Layout {
-    uint32_t x, x_stage, bars, tmem_slot, total;
+    uint32_t x, x_stage, sums, bars, tmem_slot, total;
 };
+
+// Q4_K group sums of x: a ring of kSumSlots sub-chunks, [slot][group 0..1][b_pad]
+// fp32. The X warp fills sub-chunk j only after the MMAs of j - kAStages, which
+// came after the epilogue of j - kAStages - (accumulator sets) released its set,
+// so a slot is never refilled while its readers may still need it.
+constexpr int kSumSlots = 16;
 
 __host__ __device__ inline Layout layout_for(uint32_t stage_bytes, int nraw, int nx, int b_pad) {
     Layout L;
     L.x = (uint32_t)nraw * stage_bytes;
     L.x_stage = (uint32_t)(256 * b_pad);  // four K-steps of 2 b_pad rows x 16 bf16
-    L.bars = (L.x + (uint32_t)nx * L.x_stage + 127u) & ~127u;  // nx = kAStages
-    L.tmem_slot = L.bars + 8u * (6 * kMaxStages + 2 * kAStages);
+    L.sums = L.x + (uint32_t)nx * L.x_stage;  // nx = kAStages
+    L.bars = (L.sums + (uint32_t)(kSumSlots * 2 * b_pad * 4) + 127u) & ~127u;
+    L.tmem_slot = L.bars + 8u * (6 * kMaxStages + 2 * kAStages + kSumSlots);
     L.total = L.tmem_slot + 16u;
     if (L.total < (uint32_t)kMinSmem) L.total = kMinSmem;
     return L;
@@ -201,6 +209,10 @@ QDQ_DEV float ld_dsmem_f32(uint32_t a) {
     return v;
 }
 QDQ_DEV void sts_u8(uint32_t a, uint32_t v) { asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "r"(v) : "memory"); }
+QDQ_DEV void sts128(uint32_t a, const uint32_t (&v)[4]) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
 QDQ_DEV uint32_t lds_u16(uint32_t a) {
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
@@ -437,6 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw_full = sb + L.bars, raw_empty = raw_full + 8 * kMaxStages;
     const uint32_t d_full = raw_empty + 8 * kMaxStages, d_empty = d_full + 8 * kMaxStages;
     const uint32_t a_full = d_empty + 8 * kMaxStages, a_empty = a_full + 8 * kAStages;
+    const uint32_t s_full = a_empty + 8 * kAStages;  // Q4_K group sums of a sub-chunk stored
+    const uint32_t sums_a = sb + L.sums;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nraw; ++s) {
@@ -448,12 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(d_empty + 8 * s, rr_groups(TYPE, BP) ? 4 : kDecWarps);
         }
         // an A stage is full when its decode warps (16, or the four of a group) have
-        // stored its quants and the sub-chunk's split X has landed (the X producer's
-        // arrival carries the bytes)
+        // stored its quants and the X warp has stored the sub-chunk's split x
         for (int s = 0; s < kAStages; ++s) {
             mbar_init(a_full + 8 * s, (rr_groups(TYPE, BP) ? 4 : kDecWarps) + 1);
             mbar_init(a_empty + 8 * s, 1);
         }
+        for (int s = 0; s < kSumSlots; ++s) mbar_init(s_full + 8 * s, 1);
         fence_mbar_init();
     }
     if (warp == kWarpMma) {
@@ -519,21 +533,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nbytes) bulk_g2s_hint(dst, (const void *)src_al, nbytes, raw_full + 8 * s, pol);
         }
     } else if (warp == kWarpX) {
-        // ---- split X, one bulk copy per sub-chunk, into the X slot of the A stage ---
-        if (lane == 0) {
-            Ring rx(kAStages);
-            bool ok = true;
-            int j = 0;
-            for (int u = u0; u < u1 && ok; ++u) {
-                const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-                for (int sub = 0; sub < ns; ++sub, ++j, rx.next()) {
-                    const int s = rx.slot;
-                    if (j >= kAStages && !(ok = mbar_wait(a_empty + 8 * s, rx.phase ^ 1, status))) break;
-                    const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
-                    const int64_t kstep0 = ((int64_t)u * kUnitK + kSubK * sub) / 16;
-                    const uint32_t bytes = (uint32_t)(ks * 64 * b_pad);
-                    mbar_arrive_expect_tx(a_full + 8 * s, bytes);
-                    bulk_g2s(sb + L.x + s * L.x_stage, a.xs + kstep0 * 64 * b_pad, bytes, a_full + 8 * s);
+        // ---- split X: for each sub-chunk, item (n, g) of a lane is batch row n and
+        // 32-column group g: eight float4 of x, split into bf16 hi + lo and stored
+        // in the canonical K-major layout of the X slot (x_hi rows 0..b_pad-1, x_lo
+        // rows b_pad..2 b_pad-1; rows past the batch are zero), plus (Q4_K) their
+        // sum. The loads of a lane's next item are in flight while it stores this one.
+        Ring rx(kAStages);
+        bool ok = true;
+        int j = 0;
+        constexpr int kItems = 2 * BP;
+        auto load_item = [&](int64_t c0, int ks, int it, float4 (&v)[8]) {
+            const int g = it / BP, n = it - g * BP;
+            const float *src = a.x + (int64_t)n * a.cols + c0 + 32 * g;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = (n < a.batch && 2 * g + (i >> 2) < ks) ? __ldg(reinterpret_cast<const float4 *>(src) + i)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        for (int u = u0; u < u1 && ok; ++u) {
+            const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
+            for (int sub = 0; sub < ns && ok; ++sub, ++j, rx.next()) {
+                const int s = rx.slot;
+                const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
+                const int64_t c0 = (int64_t)u * kUnitK + kSubK * sub;
+                float4 cur[8], nxt[8];
+                load_item(c0, ks, lane, cur);
+                if (j >= kAStages) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_empty + 8 * s, rx.phase ^ 1, status));
+                    if (!ok) break;
+                }
+                const uint32_t xslot = sb + L.x + (uint32_t)s * L.x_stage;
+                const uint32_t sslot = sums_a + (uint32_t)((j % kSumSlots) * 2 * BP * 4);
+#pragma unroll 1
+                for (int it = lane; it < kItems; it += 32) {
+                    if (it + 32 < kItems) load_item(c0, ks, it + 32, nxt);
+                    const int g = it / BP, n = it - g * BP;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {  // (K-step 2g + (h >> 1), 8-column half h & 1)
+                        const int t = 2 * g + (h >> 1), kk = h & 1;
+                        if (t < ks) {
+                            uint32_t hi[4], lo[4];
+                            split_pair(pack2(cur[2 * h].x, cur[2 * h].y), hi[0], lo[0]);
+                            split_pair(pack2(cur[2 * h].z, cur[2 * h].w), hi[1], lo[1]);
+                            split_pair(pack2(cur[2 * h + 1].x, cur[2 * h + 1].y), hi[2], lo[2]);
+                            split_pair(pack2(cur[2 * h + 1].z, cur[2 * h + 1].w), hi[3], lo[3]);
+                            const uint32_t blk = xslot + (uint32_t)(t * 64 * BP + kk * 128 + (n & 7) * 16);
+                            sts128(blk + (uint32_t)((n >> 3) * 256), hi);
+                            sts128(blk + (uint32_t)(((BP + n) >> 3) * 256), lo);
+                        }
+                    }
+                    if constexpr (TYPE == QDQ_Q4_K) {
+                        float acc = 0.0f;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc += (cur[i].x + cur[i].y) + (cur[i].z + cur[i].w);
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (uint32_t)((g * BP + n) * 4)), "f"(acc)
+                                     : "memory");
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+                }
+                // the MMA reads the X slot through the async proxy
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (TYPE == QDQ_Q4_K) mbar_arrive(s_full + 8 * (j % kSumSlots));
+                    mbar_arrive(a_full + 8 * s);
                 }
             }
         }
@@ -543,8 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one elected lane issues a sub-chunk's MMAs in one go, so the descriptors
         // stay in uniform registers (a lone thread issuing from per-thread registers
         // reaches a tenth of the rate). The two commits follow in their own elected
-        // block after a warp barrier: issued in the same block as the MMAs, a bounded
-        // wait ran out on one of the benchmark shapes.
+        // block after a warp barrier.
         // Per K-step t of a sub-chunk: Z_g += q x_hi and Z_g += q x_lo into the
         // accumulator region of t's group.
         const uint32_t idesc = make_idesc(b_pad), idesc2 = make_idesc(2 * b_pad);
@@ -665,20 +728,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(raw_empty + 8 * rs.slot);  // this group is done with the unit's raw data
             if (sub >= ns) continue;
-            // the sub-chunk's accumulators: set j mod nd of the MMA warp's ring. The
-            // set's previous phase (sub-chunk j - nd) is waited for first, so that the
-            // parity of this phase cannot match an older one still in flight.
+            // the sub-chunk's accumulators: set j mod nd of the MMA warp's ring, phase
+            // j / nd. In this mode nd is 4, so the set's previous phase (sub-chunk
+            // j - 4) was this group's own: it saw that phase complete and released
+            // the set before decoding j. Its next phase (j + 4) cannot complete before
+            // this group releases the set again. So the parity names this phase alone.
+            // (Waiting for the previous phase first would be wrong: when this phase
+            // has already completed, the barrier sits in the next phase, whose parity
+            // is the previous one's, and such a wait could only end with a time-out.)
             const int ds = j % nd, dp = (j / nd) & 1;
-            if (j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp ^ 1, status));
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp, status));
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * ds, dp, status));
             if (!ok) break;
             if (tr && n < 8) MTC(3, 8 * G + n);
             tc_fence_after();
+            if constexpr (TYPE == QDQ_Q4_K) {  // the X warp has stored this sub-chunk's group sums
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(s_full + 8 * (j % kSumSlots), (j / kSumSlots) & 1, status));
+                if (!ok) break;
+            }
 #pragma unroll
             for (int gi = 0; gi < kG; ++gi) {
                 // a group is present unless a short last sub-chunk (q8_0 / q4_0) ends first
                 const bool present = gi * (kSubK / kG) < uk - kSubK * sub;
-                const int gg = 8 * u + 2 * sub + gi;  // Q4_K: global 32-column group
                 const uint32_t dcol = tl + kDCol0 + (uint32_t)ds * dset + gi * gcols;
 #pragma unroll
                 for (int c8 = 0; c8 < BP / 8; ++c8) {
@@ -696,8 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (present) {
                         if constexpr (TYPE == QDQ_Q4_K) {
-                            const float4 *xg = reinterpret_cast<const float4 *>(a.xsum + (int64_t)gg * b_pad + 8 * c8);
-                            const float4 x0 = __ldg(xg), x1 = __ldg(xg + 1);
+                            const uint32_t xg = sums_a + (uint32_t)((((j % kSumSlots) * 2 + gi) * b_pad + 8 * c8) * 4);
+                            const float4 x0 = lds128f(xg), x1 = lds128f(xg + 16);
                             const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                             for (int t = 0; t < 8; ++t)
@@ -771,8 +841,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // epilogue of one sub-chunk: read back this thread's accumulator columns and
         // add s Z (- m X_g) into yacc; then release the accumulator set
-        auto epilogue = [&](float sc, float mn, int gg) -> bool {
+        auto epilogue = [&](float sc, float mn, int gg, int js) -> bool {
             if (!__all_sync(0xFFFFFFFFu, mbar_wait(d_full + 8 * rd_slot(), rd_phase(), status))) return false;
+            if constexpr (TYPE == QDQ_Q4_K) {  // the X warp has stored sub-chunk js's group sums
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(s_full + 8 * (js % kSumSlots), (js / kSumSlots) & 1, status)))
+                    return false;
+            }
             if (lane == 0 && dw < 8 && rd_count < 8) MTC(3, dw * 8 + rd_count);
             tc_fence_after();
             const uint32_t dcol = tl + kDCol0 + (uint32_t)rd_slot() * dset + grp * gcols + col0;
@@ -793,9 +867,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (gg >= 0) {
                         if constexpr (TYPE == QDQ_Q4_K) {
-                            const float4 *xg =
-                                reinterpret_cast<const float4 *>(a.xsum + (int64_t)gg * b_pad + col0 + 8 * c8);
-                            const float4 x0 = __ldg(xg), x1 = __ldg(xg + 1);
+                            const uint32_t xg =
+                                sums_a + (uint32_t)((((js % kSumSlots) * 2 + grp) * b_pad + col0 + 8 * c8) * 4);
+                            const float4 x0 = lds128f(xg), x1 = lds128f(xg + 16);
                             const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
                             for (int t = 0; t < 8; ++t) yacc[8 * c8 + t] = fmaf(sc, z[t], fmaf(-mn, xv[t], yacc[8 * c8 + t]));
@@ -875,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             const bool odd = j & 1;  // sub-chunk j - 2 has the same parity
-            if (j >= kLag) ok = odd ? epilogue(s_od, m_od, g_od) : epilogue(s_ev, m_ev, g_ev);
+            if (j >= kLag) ok = odd ? epilogue(s_od, m_od, g_od, j - kLag) : epilogue(s_ev, m_ev, g_ev, j - kLag);
             if (odd) {
                 s_od = s_new;
                 m_od = m_new;
@@ -939,55 +1013,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cluster_sync_all();
     }
     if (threadIdx.x == 0) MTR(7, 2);
-}
-
-// x[batch][cols] fp32 -> the split B operand: for each K-step t of 16 columns a
-// block of 2 b_pad rows (x_hi rows 0..b_pad-1, x_lo rows b_pad..2 b_pad-1; rows
-// past the batch are zero) in the canonical K-major layout; and, when xsum is
-// given, the sum of x over each 32-column group, xsum[group][b_pad].
-__global__ void __launch_bounds__(256) xsplit_kernel(const float *__restrict__ x, int batch, int b_pad, int64_t cols,
-                                                     uint8_t *__restrict__ xs, float *__restrict__ xsum) {
-    const int64_t total = (cols / 16) * b_pad * 2;  // (K-step, row, octet)
-    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int kk = (int)(idx & 1);
-        const int n = (int)((idx >> 1) % b_pad);
-        const int64_t t = (idx >> 1) / b_pad;
-        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
-        if (n < batch) {
-            const float4 *src = reinterpret_cast<const float4 *>(x + (int64_t)n * cols + 16 * t + 8 * kk);
-            v0 = __ldg(src);
-            v1 = __ldg(src + 1);
-        }
-        uint32_t hi[4], lo[4];
-        split_pair(pack2(v0.x, v0.y), hi[0], lo[0]);
-        split_pair(pack2(v0.z, v0.w), hi[1], lo[1]);
-        split_pair(pack2(v1.x, v1.y), hi[2], lo[2]);
-        split_pair(pack2(v1.z, v1.w), hi[3], lo[3]);
-        uint8_t *blk = xs + t * 64 * b_pad;
-        *reinterpret_cast<uint4 *>(blk + (n >> 3) * 256 + kk * 128 + (n & 7) * 16) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(blk + ((b_pad + n) >> 3) * 256 + kk * 128 + (n & 7) * 16) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    if (xsum) {
-        const int64_t ng = (cols / 32) * b_pad;
-        for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < ng;
-             idx += (int64_t)gridDim.x * blockDim.x) {
-            const int n = (int)(idx % b_pad);
-            const int64_t g = idx / b_pad;
-            float acc = 0.0f;
-            if (n < batch) {
-                const float4 *src = reinterpret_cast<const float4 *>(x + (int64_t)n * cols + 32 * g);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 v = __ldg(src + i);
-                    acc += (v.x + v.y) + (v.z + v.w);
-                }
-            }
-            xsum[idx] = acc;
-        }
-    }
 }
 
 // ---- host ----------------------------------------------------------------------------
@@ -1068,6 +1093,10 @@ int ring_depths(int type, MmaArgs &a) {
     const uint32_t dset = (uint32_t)(groups_per_sub(type) * a.b_pad * (stacked_b(type, a.b_pad) ? 2 : 1));
     a.nd = (int)std::min<uint32_t>(kMaxStages, (kTmemCols - kDCol0) / dset);
     if (a.nd < (rr_groups(type, a.b_pad) ? 4 : kLag + 1)) return QDQ_ERR_LIMIT;
+    // Four groups keep one sub-chunk each in flight, so more than four sets never
+    // fill; with exactly four, each set is only ever used by one group, which then
+    // sees every phase of it (the group's accumulator wait relies on this).
+    if (rr_groups(type, a.b_pad)) a.nd = 4;
     const Layout L0 = layout_for(a.stage_bytes, 0, a.nx, a.b_pad);
     const uint32_t fixed = L0.tmem_slot + 16u;
     a.nraw = fixed >= kSmemBudget ? 0 : (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - fixed) / a.stage_bytes);
@@ -1192,38 +1221,6 @@ int usable_cluster(int type, int want, uint32_t smem) {
     return 1;
 }
 
-// Stream-ordered scratch for the split X, from a pool of this library's own that
-// keeps its memory between calls.
-int scratch_alloc(void **p, size_t bytes, cudaStream_t stream) {
-    static std::mutex mu;
-    static cudaMemPool_t pools[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return QDQ_ERR_CUDA;
-    cudaMemPool_t pool;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!pools[dev]) {
-            cudaMemPoolProps props = {};
-            props.allocType = cudaMemAllocationTypePinned;
-            props.location.type = cudaMemLocationTypeDevice;
-            props.location.id = dev;
-            if (cudaMemPoolCreate(&pools[dev], &props) != cudaSuccess) {
-                cudaGetLastError();
-                pools[dev] = nullptr;
-                return QDQ_ERR_CUDA;
-            }
-            uint64_t keep = ~0ull;
-            cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold, &keep);
-        }
-        pool = pools[dev];
-    }
-    if (cudaMallocFromPoolAsync(p, bytes, pool, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return QDQ_ERR_CUDA;
-    }
-    return QDQ_OK;
-}
-
 int mma_cluster_size(int64_t rows, int64_t cols, int sm_count) {
     const int64_t tiles = (rows + kM - 1) / kM;
     const int64_t nunits = (cols + kUnitK - 1) / kUnitK;
@@ -1251,35 +1248,16 @@ int launch_mma_gemv(int type, const void *W, int64_t rows, int64_t cols, const f
     a.cols = cols;
     a.nunits = (int)((cols + kUnitK - 1) / kUnitK);
     const int bmax = max_bpad(type);
-    const int first = batch < bmax ? batch : bmax;
-    const int bpad_max = (first + 15) / 16 * 16;
-    const size_t split_bytes = (size_t)4 * bpad_max * cols;
-    const size_t sum_bytes = type == QDQ_Q4_K ? (size_t)(cols / 32) * bpad_max * sizeof(float) : 0;
-    void *xs = nullptr;
-    if ((rc = scratch_alloc(&xs, split_bytes + sum_bytes, stream))) return rc;
-    a.xs = (const uint8_t *)xs;
-    a.xsum = sum_bytes ? reinterpret_cast<const float *>((const uint8_t *)xs + split_bytes) : nullptr;
     for (int b0 = 0; b0 < batch && rc == QDQ_OK; b0 += bmax) {
         const int bc = batch - b0 < bmax ? batch - b0 : bmax;
         a.batch = bc;
         a.b_pad = (bc + 15) / 16 * 16;
+        a.x = x + (int64_t)b0 * cols;
         a.y = y + (int64_t)b0 * rows;
         if ((rc = ring_depths(type, a))) break;
         const uint32_t smem = layout_for(a.stage_bytes, a.nraw, a.nx, a.b_pad).total;
         const int S = usable_cluster(type, mma_cluster_size(rows, cols, sm_count), smem);
-        const int64_t work = (cols / 16) * a.b_pad * 2;
-        const int grid = (int)std::min<int64_t>((work + 255) / 256, (int64_t)sm_count * 8);
-        xsplit_kernel<<<grid, 256, 0, stream>>>(x + (int64_t)b0 * cols, bc, a.b_pad, cols, (uint8_t *)xs,
-                                                const_cast<float *>(a.xsum));
-        if (cudaGetLastError() != cudaSuccess) {
-            rc = QDQ_ERR_CUDA;
-            break;
-        }
         rc = dispatch(type, a, map, S, tiles, stream);
-    }
-    if (cudaFreeAsync(xs, stream) != cudaSuccess) {
-        cudaGetLastError();
-        if (rc == QDQ_OK) rc = QDQ_ERR_CUDA;
     }
     return rc;
 }
