@@ -184,3 +184,39 @@ def llama_1b_step(n_layers: int = 22) -> list[list[Gemv]]:
 
 def step_weight_bytes(levels: list[list[Gemv]]) -> int:
     return sum(g.weight_bytes for lv in levels for g in lv)
+
+
+# ---------------------------------------------------------------------------
+# A whole Llama-architecture model of random blocks, for the decode-step glue.
+# Tensor types follow the Q4_K_M mix above; norm weights are fp32 ~ U[0.5, 1.5].
+# ---------------------------------------------------------------------------
+LAYER_TENSORS = ("q", "k", "v", "o", "gate", "up", "down")
+LAYER_TYPES = {"q": Q4_K, "k": Q4_K, "v": Q6_K, "o": Q4_K, "gate": Q4_K, "up": Q4_K, "down": Q6_K}
+
+
+def llama_shapes(dim: int, hidden: int, n_heads: int, n_kv_heads: int) -> dict:
+    """(rows, cols) of each layer tensor: weights stored out x in."""
+    kv = n_kv_heads * (dim // n_heads)
+    return {"q": (dim, dim), "k": (kv, dim), "v": (kv, dim), "o": (dim, dim),
+            "gate": (hidden, dim), "up": (hidden, dim), "down": (dim, hidden)}
+
+
+def gen_llama_model(dim: int, hidden: int, n_layers: int, n_heads: int, n_kv_heads: int, vocab: int,
+                    seed: int, embd_type: int = Q4_K, out_type: int = Q6_K) -> dict:
+    """Raw blocks of every tensor and the fp32 norm vectors, from one seed."""
+    rng = np.random.default_rng(seed)
+    shapes = llama_shapes(dim, hidden, n_heads, n_kv_heads)
+    m = {"token_embd": (embd_type, vocab, dim, gen_blocks(embd_type, vocab * dim // BLOCK_WEIGHTS[embd_type], rng)),
+         "layers": []}
+    for _ in range(n_layers):
+        lw = {}
+        for name in LAYER_TENSORS:
+            r, c = shapes[name]
+            t = LAYER_TYPES[name]
+            lw[name] = (t, r, c, gen_blocks(t, r * c // BLOCK_WEIGHTS[t], rng))
+        lw["attn_norm"] = rng.uniform(0.5, 1.5, dim).astype(np.float32)
+        lw["ffn_norm"] = rng.uniform(0.5, 1.5, dim).astype(np.float32)
+        m["layers"].append(lw)
+    m["output_norm"] = rng.uniform(0.5, 1.5, dim).astype(np.float32)
+    m["output"] = (out_type, vocab, dim, gen_blocks(out_type, vocab * dim // BLOCK_WEIGHTS[out_type], rng))
+    return m
