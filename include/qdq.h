@@ -136,6 +136,46 @@ int qdq_gemv_group(const qdq_gemv_desc *descs, int n, int batch, qdq_stream_t st
 typedef struct qdq_plan qdq_plan;
 int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int batch,
                     qdq_plan **plan_out);
+
+/* ---------------------------------------------------------------------------
+ * Step glue fused into a plan's GEMVs ("S21 The Capstone: picoLM, in Python",
+ * section 4, model_forward: rmsnorm before the q/k/v and gate/up projections,
+ * SwiGLU between gate/up and down, residual additions after the output and down
+ * projections, and the output head whose largest logit greedy decoding takes;
+ * "PETIT", What makes it fast & small: RMSNorm + SwiGLU Llama block).
+ * opts[i] applies to descs[i]:
+ *   x_op  QDQ_X_PLAIN    the GEMV reads x as given.
+ *         QDQ_X_RMSNORM  it reads x / sqrt(mean(x^2) + eps) * norm_w (the mean
+ *                        over the cols entries of each batch column), computed
+ *                        while x is staged; norm_w is [cols] fp32.
+ *         QDQ_X_SWIGLU   it reads silu(x) * x2 with silu(g) = g / (1 + exp(-g));
+ *                        x is the gate output, x2 the up output, both
+ *                        [batch][cols].
+ *   y_op  QDQ_Y_STORE    y = W x' (as qdq_gemv).
+ *         QDQ_Y_ADD      y += W x' (a residual addition; y must not be read by
+ *                        another GEMV of the same level).
+ *   argmax  NULL, or a device int64: after the run it holds the index of the
+ *           largest y of this GEMV (the smallest such index on ties). At most
+ *           one GEMV of a plan, in its last level, batch 1, cols <= 8192.
+ * GEMVs of one level that read the same x must use the same x_op, x2, norm_w
+ * and eps. Every option is applied inside the plan's single kernel: no pass of
+ * its own. Errors: QDQ_ERR_SHAPE for a rule above broken, QDQ_ERR_PTR /
+ * QDQ_ERR_ALIGN for a bad x2, norm_w or argmax pointer. The plan then also
+ * owns 16 bytes of device memory for the argmax.
+ * ------------------------------------------------------------------------- */
+enum qdq_x_op { QDQ_X_PLAIN = 0, QDQ_X_RMSNORM = 1, QDQ_X_SWIGLU = 2 };
+enum qdq_y_op { QDQ_Y_STORE = 0, QDQ_Y_ADD = 1 };
+typedef struct qdq_gemv_opts {
+    int32_t x_op;
+    int32_t y_op;
+    const float *x2;
+    const float *norm_w;
+    float eps;
+    int32_t reserved;
+    int64_t *argmax;
+} qdq_gemv_opts;
+int qdq_plan_create_ex(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n,
+                       int batch, qdq_plan **plan_out);
 int qdq_plan_run(qdq_plan *plan, qdq_stream_t stream);
 /* The same run with host I/O: copies x_host (every distinct x buffer of the
  * plan, concatenated in order of first use, each [batch][cols]) to the plan's x
@@ -167,6 +207,71 @@ int qdq_plan_launches(const qdq_plan *plan);
  * ------------------------------------------------------------------------- */
 int qdq_gemv_levels_noalloc(const qdq_gemv_desc *descs, const int *level, int n, int batch,
                             qdq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * qdq_rope_attention: the attention block of one decode position
+ * ("S21 The Capstone: picoLM, in Python", section 4, model_forward, and section
+ * 3 for the RoPE layout; "PETIT", How the pieces match: RoPE base, per head).
+ *   1. RoPE in the interleaved layout: within each head, the pair
+ *      (v[2i], v[2i+1]) of q and of k turns by pos * rope_base^(-2i/head_dim).
+ *   2. The cache is fp16: the turned k and the v of this position are rounded
+ *      to fp16 (to nearest even) and stored at row pos of k_cache / v_cache.
+ *   3. For each query head h, with KV head g = h / (n_heads / n_kv_heads):
+ *      out_h = sum_{t <= pos} p_t v_t, p = softmax_t(k_t . q_h / sqrt(head_dim)),
+ *      every k_t, v_t in its fp16 value. Online softmax in fp32 (no score array).
+ * q: [n_heads * head_dim]; k, v: [n_kv_heads * head_dim]; out: [n_heads *
+ * head_dim], fp32 device buffers. k_cache, v_cache: [max_seq][n_kv_heads *
+ * head_dim] fp16 bit patterns, device, owned by the caller; rows < pos must hold
+ * earlier positions. head_dim even and <= 256, n_heads a multiple of n_kv_heads,
+ * 0 <= pos < max_seq (else QDQ_ERR_SHAPE). One launch of n_heads CTAs.
+ * ------------------------------------------------------------------------- */
+int qdq_rope_attention(const float *q, const float *k, const float *v, uint16_t *k_cache,
+                       uint16_t *v_cache, float *out, int n_heads, int n_kv_heads, int head_dim,
+                       int pos, int max_seq, float rope_base, qdq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * A one-token forward pass of a Llama-architecture model over block-quantised
+ * weights ("S21 The Capstone: picoLM, in Python", section 4, model_forward(m,
+ * token, pos)): h = the token's embedding row (decoded); per layer
+ *   h += Wo attention(rope(Wq n), rope(Wk n), Wv n),  n = rmsnorm(h, attn_norm)
+ *   h += Wdown (silu(Wgate n') * Wup n'),              n' = rmsnorm(h, ffn_norm)
+ * then logits = Wout rmsnorm(h, output_norm) and their argmax.
+ * The embedding's row length in bytes must be a multiple of 16 (QDQ_ERR_ALIGN).
+ * Weights are out x in (rows x cols) blocks of any of the four types, device
+ * memory owned by the caller, which must outlive the model. layer.w[] and
+ * layer.type[] are in the order q, k, v, o, gate, up, down with shapes q, o:
+ * dim x dim; k, v: kv x dim (kv = n_kv_heads * dim / n_heads); gate, up:
+ * hidden x dim; down: dim x hidden. Norm weights are fp32 device vectors [dim].
+ * The model allocates its activations, the fp16 key/value cache
+ * ([n_layers][max_seq][kv] each) and its plans in create, and frees them in
+ * destroy. A forward call runs 2 + 2 n_layers launches on `stream`: the
+ * embedding row's decode, the first layer's q/k/v, then per layer the attention
+ * launch and one plan (o, gate/up, down, next q/k/v or the head). Positions
+ * must be run in order 0, 1, ... (a position reads the cache rows before it).
+ * qdq_llama_buffers returns the device addresses of the logits [vocab], argmax
+ * (one int64), the residual stream h [dim] and the two caches.
+ * ------------------------------------------------------------------------- */
+typedef struct qdq_llama_config {
+    int32_t dim, hidden, n_layers, n_heads, n_kv_heads, vocab, max_seq, reserved;
+    float rope_base; /* 10000 in PETIT */
+    float norm_eps;  /* rmsnorm epsilon */
+} qdq_llama_config;
+typedef struct qdq_llama_layer {
+    const void *w[7];
+    int32_t type[7];
+    int32_t reserved;
+    const float *attn_norm;
+    const float *ffn_norm;
+} qdq_llama_layer;
+typedef struct qdq_llama qdq_llama;
+int qdq_llama_create(const qdq_llama_config *cfg, const void *token_embd, int embd_type,
+                     const qdq_llama_layer *layers, const float *output_norm, const void *output,
+                     int output_type, qdq_llama **model_out);
+int qdq_llama_forward(qdq_llama *model, int token, int pos, qdq_stream_t stream);
+int qdq_llama_buffers(const qdq_llama *model, float **logits, int64_t **argmax, float **hidden,
+                      uint16_t **k_cache, uint16_t **v_cache);
+int qdq_llama_launches(const qdq_llama *model);
+void qdq_llama_destroy(qdq_llama *model);
 
 /* ---------------------------------------------------------------------------
  * Device status: synchronises `stream`, returns the first device-side error

@@ -59,7 +59,8 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float = EPS) -> np.ndarray:
 
 def silu(g: np.ndarray) -> np.ndarray:
     g = np.asarray(g, dtype=np.float64)
-    return g / (1.0 + np.exp(-g))
+    with np.errstate(over="ignore"):  # exp(-g) = inf below g = -709: g / inf is the limit, -0
+        return g / (1.0 + np.exp(-g))
 
 
 def swiglu(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
@@ -199,13 +200,20 @@ def fp16_round(v: np.ndarray) -> np.ndarray:
 
 
 def forward(m: LlamaWeights, k_cache: np.ndarray, v_cache: np.ndarray, token: int, pos: int,
-            trace: dict | None = None) -> np.ndarray:
+            trace: dict | None = None, rows: dict | None = None) -> np.ndarray:
     """Logits of one token at position `pos` [S21-4 model_forward / forward].
 
     k_cache, v_cache: float16 [n_layers][max_seq][kv_dim]; entries of positions
     < pos are read, and position pos is written (the key after RoPE). If `trace`
     is a dict, the unrounded key and value of each layer, the residual stream
-    after the last layer and its norm go into it."""
+    after the last layer and its norm go into it.
+
+    Rounding a key or value to fp16 is a decision on a discrete value: a kernel
+    that computes k in fp32 can land on the neighbouring fp16 value when k sits
+    near a rounding boundary. `rows` ({"k": [layer][kv_dim], "v": ...} fp16)
+    gives the row each layer stores at `pos` instead of fp16(k), fp16(v), so a
+    comparison takes that decision once, on the kernel's side, after checking
+    the kernel's rows against the unrounded values traced here."""
     c = m.cfg
     x = m.token_embd.row(token)
     for l in range(c.n_layers):
@@ -218,8 +226,8 @@ def forward(m: LlamaWeights, k_cache: np.ndarray, v_cache: np.ndarray, token: in
         if trace is not None:
             trace.setdefault("k", []).append(k)
             trace.setdefault("v", []).append(v)
-        k_cache[l, pos] = fp16_round(k)  # the cache is fp16
-        v_cache[l, pos] = fp16_round(v)
+        k_cache[l, pos] = fp16_round(k) if rows is None else rows["k"][l]  # the cache is fp16
+        v_cache[l, pos] = fp16_round(v) if rows is None else rows["v"][l]
         att = attention(q, k_cache[l].reshape(c.max_seq, c.n_kv_heads, c.head_dim),
                         v_cache[l].reshape(c.max_seq, c.n_kv_heads, c.head_dim), pos + 1,
                         c.n_heads, c.n_kv_heads, c.head_dim)

@@ -109,6 +109,7 @@ using namespace qdq;
 struct qdq_plan {
     StreamPlanHost *host = nullptr;
     unsigned *counters = nullptr;
+    unsigned long long *amax = nullptr;  // argmax slot (plans with an argmax option)
     int device = -1;
     int n = 0, batch = 1, nlevels = 1;
     std::vector<qdq_gemv_desc> descs;
@@ -174,7 +175,7 @@ int qdq_dequant(int type, const void *blocks, int64_t n, float *out_f32) {
 
 static int run_stream_once(const qdq_gemv_desc *descs, int n, int batch, cudaStream_t stream, int sm_count) {
     StreamPlanHost *p = nullptr;
-    int rc = stream_plan_build(descs, nullptr, n, batch, nullptr, sm_count, &p);
+    int rc = stream_plan_build(descs, nullptr, nullptr, n, batch, nullptr, nullptr, sm_count, &p);
     if (rc) return rc;
     rc = stream_plan_launch(p, stream);
     stream_plan_free(p);
@@ -220,6 +221,42 @@ int qdq_gemv_group(const qdq_gemv_desc *descs, int n, int batch, qdq_stream_t st
 }
 
 int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int batch, qdq_plan **plan_out) {
+    return qdq_plan_create_ex(descs, nullptr, level, n, batch, plan_out);
+}
+
+// The rules of qdq_gemv_opts (include/qdq.h).
+static int check_opts(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n, int batch,
+                      int device, bool *has_argmax) {
+    *has_argmax = false;
+    if (opts == nullptr) return QDQ_OK;
+    int rc = QDQ_OK;
+    for (int i = 0; i < n && !rc; ++i) {
+        const qdq_gemv_opts &o = opts[i];
+        if (o.x_op < QDQ_X_PLAIN || o.x_op > QDQ_X_SWIGLU || o.y_op < QDQ_Y_STORE || o.y_op > QDQ_Y_ADD)
+            return QDQ_ERR_SHAPE;
+        if (o.x_op == QDQ_X_RMSNORM) {
+            if (!(o.eps >= 0.0f) || o.eps > 1.0f) return QDQ_ERR_SHAPE;
+            rc = check_dev_ptr(o.norm_w, device);
+        }
+        if (!rc && o.x_op == QDQ_X_SWIGLU) rc = check_dev_ptr(o.x2, device);
+        if (!rc && o.argmax) {
+            if (*has_argmax || batch != 1 || level[i] != level[n - 1] || descs[i].cols > 8192) return QDQ_ERR_SHAPE;
+            if (descs[i].rows > 0xFFFFFFFFll) return QDQ_ERR_SHAPE;
+            rc = check_dev_ptr(o.argmax, device);
+            *has_argmax = true;
+        }
+        // GEMVs of one level reading the same x stage it once: same x option
+        for (int k = 0; k < i && !rc; ++k)
+            if (level[k] == level[i] && descs[k].x == descs[i].x &&
+                (opts[k].x_op != o.x_op || (o.x_op == QDQ_X_SWIGLU && opts[k].x2 != o.x2) ||
+                 (o.x_op == QDQ_X_RMSNORM && (opts[k].norm_w != o.norm_w || opts[k].eps != o.eps))))
+                return QDQ_ERR_SHAPE;
+    }
+    return rc;
+}
+
+int qdq_plan_create_ex(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n, int batch,
+                       qdq_plan **plan_out) {
     if (plan_out == nullptr || level == nullptr) return QDQ_ERR_PTR;
     *plan_out = nullptr;
     if (n < 1 || n > kMaxPlanDescs) return QDQ_ERR_LIMIT;
@@ -231,6 +268,8 @@ int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int bat
     const DeviceInfo &dev = current_device(&rc);
     if (rc) return rc;
     if ((rc = check_descs(descs, n, batch, dev.device))) return rc;
+    bool has_argmax = false;
+    if ((rc = check_opts(descs, opts, level, n, batch, dev.device, &has_argmax))) return rc;
     qdq_plan *p = new (std::nothrow) qdq_plan();
     if (!p) return QDQ_ERR_CUDA;
     p->device = dev.device;
@@ -238,18 +277,21 @@ int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int bat
     p->batch = batch;
     p->nlevels = nlevels;
     p->descs.assign(descs, descs + n);
-    if (cudaMalloc((void **)&p->counters, sizeof(unsigned) * nlevels) != cudaSuccess ||
-        cudaMemset(p->counters, 0, sizeof(unsigned) * nlevels) != cudaSuccess) {
+    auto fail = [&](int code) {
         cudaGetLastError();
         if (p->counters) cudaFree(p->counters);
+        if (p->amax) cudaFree(p->amax);
         delete p;
-        return QDQ_ERR_CUDA;
-    }
-    if ((rc = stream_plan_build(descs, level, n, batch, p->counters, dev.sm_count, &p->host))) {
-        cudaFree(p->counters);
-        delete p;
-        return rc;
-    }
+        return code;
+    };
+    if (cudaMalloc((void **)&p->counters, sizeof(unsigned) * nlevels) != cudaSuccess ||
+        cudaMemset(p->counters, 0, sizeof(unsigned) * nlevels) != cudaSuccess)
+        return fail(QDQ_ERR_CUDA);
+    if (has_argmax && (cudaMalloc((void **)&p->amax, 2 * sizeof(unsigned long long)) != cudaSuccess ||
+                       cudaMemset(p->amax, 0, 2 * sizeof(unsigned long long)) != cudaSuccess))
+        return fail(QDQ_ERR_CUDA);
+    if ((rc = stream_plan_build(descs, opts, level, n, batch, p->counters, p->amax, dev.sm_count, &p->host)))
+        return fail(rc);
     *plan_out = p;
     return QDQ_OK;
 }
@@ -307,15 +349,19 @@ int qdq_plan_run_io(qdq_plan *plan, const float *x_host, float *y_host, qdq_stre
 
 int qdq_plan_reset(qdq_plan *plan, qdq_stream_t stream) {
     if (plan == nullptr) return QDQ_ERR_PTR;
-    return cudaMemsetAsync(plan->counters, 0, sizeof(unsigned) * plan->nlevels, (cudaStream_t)stream) == cudaSuccess
-               ? QDQ_OK
-               : QDQ_ERR_CUDA;
+    if (cudaMemsetAsync(plan->counters, 0, sizeof(unsigned) * plan->nlevels, (cudaStream_t)stream) != cudaSuccess ||
+        (plan->amax && cudaMemsetAsync(plan->amax, 0, 2 * sizeof(unsigned long long), (cudaStream_t)stream) != cudaSuccess)) {
+        cudaGetLastError();
+        return QDQ_ERR_CUDA;
+    }
+    return QDQ_OK;
 }
 
 void qdq_plan_destroy(qdq_plan *plan) {
     if (plan == nullptr) return;
     stream_plan_free(plan->host);
     if (plan->counters) cudaFree(plan->counters);
+    if (plan->amax) cudaFree(plan->amax);
     delete plan;
 }
 

@@ -26,8 +26,11 @@ int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStre
 
 // The streaming (CUDA-core) GEMV over a list of GEMVs grouped in dependency levels.
 struct StreamPlanHost;  // opaque: the packed kernel arguments
-int stream_plan_build(const qdq_gemv_desc *descs, const int *level, int n, int batch,
-                      unsigned *counters, int sm_count, StreamPlanHost **out);
+// opts (may be NULL: every GEMV plain) and amax_slot (two zeroed 64-bit words,
+// needed when an option asks for an argmax) as for qdq_plan_create_ex.
+int stream_plan_build(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n,
+                      int batch, unsigned *counters, unsigned long long *amax_slot, int sm_count,
+                      StreamPlanHost **out);
 int stream_plan_launch(const StreamPlanHost *p, cudaStream_t stream);
 void stream_plan_free(StreamPlanHost *p);
 int stream_plan_nlevels(const StreamPlanHost *p);

@@ -1,0 +1,365 @@
+// qdq_llama.cu -- the decode-step glue around the GEMV plans: the attention block
+// of one position (RoPE, fp16 key/value cache, GQA attention with an online
+// softmax) and a one-token forward pass of a Llama-architecture model built from
+// plans whose GEMVs carry the rmsnorm, SwiGLU, residual and argmax options.
+//
+// "S21 The Capstone: picoLM, in Python", section 4 (model_forward(m, token, pos):
+// the embedding row, per layer rmsnorm -> q/k/v -> rope -> fp16 cache at pos ->
+// per-head attention with an online softmax and GQA -> output projection ->
+// SwiGLU -> residuals; final rmsnorm and output matmul) and section 3 (the
+// interleaved RoPE layout: pairs (x[2i], x[2i+1])); "PETIT", How the pieces match
+// (RoPE base 10000, applied per head).
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_fp16.h>
+
+#include "qdq_internal.h"
+
+namespace qdq {
+namespace {
+
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kMaxHeadDim = 256;
+
+// One CTA per query head h (KV head g = h / kv_mul).
+//  1. Angles of the pairs in double precision: pos * base^(-2i / head_dim) reaches
+//     thousands of radians, where a float angle would be off by 1e-4.
+//  2. q_h and k_g turn pair by pair; k and v are rounded to fp16 (the cache is
+//     fp16), and the first query head of the group stores them at position pos.
+//  3. Online softmax over t <= pos: warp w takes t = w, w + 8, ...; each keeps a
+//     running maximum m, sum l and weighted value sum, rescaled when m grows;
+//     the warps' states are merged at the end. No score array exists. The
+//     current position's key and value come from shared memory (their fp16
+//     values), so no CTA reads a cache entry another CTA is writing.
+__global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__restrict__ q, const float *__restrict__ k,
+                                                                 const float *__restrict__ v, __half *k_cache,
+                                                                 __half *v_cache, float *__restrict__ out,
+                                                                 int n_heads, int n_kv_heads, int D, int pos,
+                                                                 float rope_base) {
+    __shared__ float qs[kMaxHeadDim], kc[kMaxHeadDim], vc[kMaxHeadDim];
+    __shared__ float wm[kAttnWarps], wl[kAttnWarps];
+    __shared__ float wacc[kAttnWarps][kMaxHeadDim];
+    const int h = blockIdx.x, kv_mul = n_heads / n_kv_heads, g = h / kv_mul;
+    const int kvd = n_kv_heads * D;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool writer = (h % kv_mul) == 0;
+
+    for (int i = tid; i < D / 2; i += kAttnThreads) {
+        const double th = (double)pos * pow((double)rope_base, -2.0 * (double)i / (double)D);
+        const float c = (float)cos(th), s = (float)sin(th);
+        const float qa = q[h * D + 2 * i], qb = q[h * D + 2 * i + 1];
+        qs[2 * i] = qa * c - qb * s;
+        qs[2 * i + 1] = qa * s + qb * c;
+        const float ka = k[g * D + 2 * i], kb = k[g * D + 2 * i + 1];
+        const __half k0 = __float2half_rn(ka * c - kb * s), k1 = __float2half_rn(ka * s + kb * c);
+        const __half v0 = __float2half_rn(v[g * D + 2 * i]), v1 = __float2half_rn(v[g * D + 2 * i + 1]);
+        kc[2 * i] = __half2float(k0);
+        kc[2 * i + 1] = __half2float(k1);
+        vc[2 * i] = __half2float(v0);
+        vc[2 * i + 1] = __half2float(v1);
+        if (writer) {
+            const int64_t o = (int64_t)pos * kvd + g * D + 2 * i;
+            k_cache[o] = k0;
+            k_cache[o + 1] = k1;
+            v_cache[o] = v0;
+            v_cache[o + 1] = v1;
+        }
+    }
+    __syncthreads();
+
+    const float inv = 1.0f / sqrtf((float)D);
+    constexpr int kPer = kMaxHeadDim / 32;  // dims per lane: d = lane + 32 j
+    float m = -INFINITY, l = 0.f, acc[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+    for (int t = warp; t <= pos; t += kAttnWarps) {
+        const __half *kr = k_cache + (int64_t)t * kvd + g * D;
+        const __half *vr = v_cache + (int64_t)t * kvd + g * D;
+        float dot = 0.f;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int d = lane + 32 * j;
+            if (d < D) dot += qs[d] * (t == pos ? kc[d] : __half2float(kr[d]));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
+        const float s = dot * inv;
+        const float mn = fmaxf(m, s);
+        const float scale = expf(m - mn), p = expf(s - mn);
+        l = l * scale + p;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int d = lane + 32 * j;
+            if (d < D) acc[j] = acc[j] * scale + p * (t == pos ? vc[d] : __half2float(vr[d]));
+        }
+        m = mn;
+    }
+    if (lane == 0) {
+        wm[warp] = m;
+        wl[warp] = l;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int d = lane + 32 * j;
+        if (d < D) wacc[warp][d] = acc[j];
+    }
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w]);
+    float L = 0.f;
+    for (int w = 0; w < kAttnWarps; ++w)
+        if (wl[w] > 0.f) L += wl[w] * expf(wm[w] - M);
+    for (int d = tid; d < D; d += kAttnThreads) {
+        float o = 0.f;
+        for (int w = 0; w < kAttnWarps; ++w)
+            if (wl[w] > 0.f) o += wacc[w][d] * expf(wm[w] - M);
+        out[h * D + d] = o / L;
+    }
+}
+
+}  // namespace
+
+int launch_rope_attention(const float *q, const float *k, const float *v, uint16_t *k_cache, uint16_t *v_cache,
+                          float *out, int n_heads, int n_kv_heads, int head_dim, int pos, float rope_base,
+                          cudaStream_t stream) {
+    rope_attn_kernel<<<n_heads, kAttnThreads, 0, stream>>>(q, k, v, (__half *)k_cache, (__half *)v_cache, out,
+                                                           n_heads, n_kv_heads, head_dim, pos, rope_base);
+    if (cudaGetLastError() != cudaSuccess) return QDQ_ERR_CUDA;
+    return QDQ_OK;
+}
+
+}  // namespace qdq
+
+using namespace qdq;
+
+// A model instance: the caller's weights, the library's activations, fp16 cache
+// and plans. Buffers in one device allocation:
+//   h[dim] (residual stream), q[dim], k[kv], v[kv], att[dim], gate[hidden],
+//   up[hidden], logits[vocab], argmax (int64), then the key and value caches
+//   [n_layers][max_seq][kv] fp16.
+struct qdq_llama {
+    qdq_llama_config cfg{};
+    int device = -1;
+    const void *embd = nullptr;
+    int embd_type = 0;
+    int64_t embd_row_bytes = 0;
+    char *mem = nullptr;
+    float *h = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *att = nullptr, *gate = nullptr, *up = nullptr,
+          *logits = nullptr;
+    int64_t *argmax = nullptr;
+    uint16_t *kcache = nullptr, *vcache = nullptr;
+    qdq_plan *first = nullptr;             // q/k/v of layer 0
+    std::vector<qdq_plan *> layer_plans;  // layer l: o, gate/up, down, then q/k/v of l+1 or the head
+};
+
+namespace {
+
+int64_t align256(int64_t b) { return (b + 255) / 256 * 256; }
+
+int check_config(const qdq_llama_config *c) {
+    if (c->dim < 1 || c->hidden < 1 || c->n_layers < 1 || c->n_heads < 1 || c->n_kv_heads < 1 || c->vocab < 1 ||
+        c->max_seq < 1)
+        return QDQ_ERR_SHAPE;
+    if (c->dim % c->n_heads || c->n_heads % c->n_kv_heads) return QDQ_ERR_SHAPE;
+    const int D = c->dim / c->n_heads;
+    if (D % 2 || D > kMaxHeadDim) return QDQ_ERR_SHAPE;
+    if (!(c->rope_base > 1.0f) || !(c->norm_eps >= 0.0f)) return QDQ_ERR_SHAPE;
+    if (c->n_layers > 1024 || c->vocab > (1 << 30) || c->max_seq > (1 << 24)) return QDQ_ERR_LIMIT;
+    return QDQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qdq_rope_attention(const float *q, const float *k, const float *v, uint16_t *k_cache, uint16_t *v_cache,
+                       float *out, int n_heads, int n_kv_heads, int head_dim, int pos, int max_seq, float rope_base,
+                       qdq_stream_t stream) {
+    if (n_heads < 1 || n_kv_heads < 1 || n_heads % n_kv_heads || head_dim < 2 || head_dim % 2 ||
+        head_dim > kMaxHeadDim || pos < 0 || pos >= max_seq || !(rope_base > 1.0f))
+        return QDQ_ERR_SHAPE;
+    if (!q || !k || !v || !k_cache || !v_cache || !out) return QDQ_ERR_PTR;
+    int rc = QDQ_OK;
+    current_device(&rc);
+    if (rc) return rc;
+    return launch_rope_attention(q, k, v, k_cache, v_cache, out, n_heads, n_kv_heads, head_dim, pos, rope_base,
+                                 (cudaStream_t)stream);
+}
+
+int qdq_llama_create(const qdq_llama_config *cfg, const void *token_embd, int embd_type,
+                     const qdq_llama_layer *layers, const float *output_norm, const void *output, int output_type,
+                     qdq_llama **out) {
+    if (out == nullptr || cfg == nullptr || layers == nullptr || token_embd == nullptr || output_norm == nullptr ||
+        output == nullptr)
+        return QDQ_ERR_PTR;
+    *out = nullptr;
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    const DeviceInfo &dev = current_device(&rc);
+    if (rc) return rc;
+    if (qdq_block_weights(embd_type) <= 0 || qdq_block_weights(output_type) <= 0) return QDQ_ERR_TYPE;
+    if (cfg->dim % qdq_block_weights(embd_type)) return QDQ_ERR_SHAPE;
+    // the embedding row is decoded in place: its first byte must be 16-byte aligned
+    if (((int64_t)cfg->dim / qdq_block_weights(embd_type) * qdq_block_bytes(embd_type)) % 16) return QDQ_ERR_ALIGN;
+    qdq_llama *m = new (std::nothrow) qdq_llama();
+    if (!m) return QDQ_ERR_CUDA;
+    m->cfg = *cfg;
+    m->device = dev.device;
+    m->embd = token_embd;
+    m->embd_type = embd_type;
+    m->embd_row_bytes = (int64_t)cfg->dim / qdq_block_weights(embd_type) * qdq_block_bytes(embd_type);
+    const int64_t dim = cfg->dim, hid = cfg->hidden, kv = (int64_t)cfg->n_kv_heads * (cfg->dim / cfg->n_heads);
+    const int64_t cache = (int64_t)cfg->n_layers * cfg->max_seq * kv * 2;
+    int64_t off[11], total = 0;
+    const int64_t sizes[11] = {4 * dim, 4 * dim, 4 * kv, 4 * kv, 4 * dim, 4 * hid, 4 * hid, 4 * (int64_t)cfg->vocab,
+                               8, cache, cache};
+    for (int i = 0; i < 11; ++i) {
+        off[i] = total;
+        total += align256(sizes[i]);
+    }
+    if (cudaMalloc((void **)&m->mem, total) != cudaSuccess || cudaMemset(m->mem, 0, total) != cudaSuccess) {
+        cudaGetLastError();
+        if (m->mem) cudaFree(m->mem);
+        delete m;
+        return QDQ_ERR_CUDA;
+    }
+    m->h = (float *)(m->mem + off[0]);
+    m->q = (float *)(m->mem + off[1]);
+    m->k = (float *)(m->mem + off[2]);
+    m->v = (float *)(m->mem + off[3]);
+    m->att = (float *)(m->mem + off[4]);
+    m->gate = (float *)(m->mem + off[5]);
+    m->up = (float *)(m->mem + off[6]);
+    m->logits = (float *)(m->mem + off[7]);
+    m->argmax = (int64_t *)(m->mem + off[8]);
+    m->kcache = (uint16_t *)(m->mem + off[9]);
+    m->vcache = (uint16_t *)(m->mem + off[10]);
+
+    const float eps = cfg->norm_eps;
+    auto desc = [](int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y) {
+        qdq_gemv_desc d;
+        std::memset(&d, 0, sizeof(d));
+        d.type = type;
+        d.W = W;
+        d.rows = rows;
+        d.cols = cols;
+        d.x = x;
+        d.y = y;
+        return d;
+    };
+    auto opt = [](int x_op, int y_op, const float *x2, const float *nw, float e, int64_t *am) {
+        qdq_gemv_opts o;
+        std::memset(&o, 0, sizeof(o));
+        o.x_op = x_op;
+        o.y_op = y_op;
+        o.x2 = x2;
+        o.norm_w = nw;
+        o.eps = e;
+        o.argmax = am;
+        return o;
+    };
+    std::vector<qdq_gemv_desc> D;
+    std::vector<qdq_gemv_opts> O;
+    std::vector<int> Lv;
+    // q, k, v of layer l read rmsnorm(h, attn_norm[l]) (one staged x for the three)
+    auto add_qkv = [&](int l, int level) {
+        const qdq_llama_layer &w = layers[l];
+        const float *nw = w.attn_norm;
+        D.push_back(desc(w.type[0], w.w[0], dim, dim, m->h, m->q));
+        D.push_back(desc(w.type[1], w.w[1], kv, dim, m->h, m->k));
+        D.push_back(desc(w.type[2], w.w[2], kv, dim, m->h, m->v));
+        for (int i = 0; i < 3; ++i) {
+            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, nw, eps, nullptr));
+            Lv.push_back(level);
+        }
+    };
+    auto make = [&](qdq_plan **p) {
+        const int r = qdq_plan_create_ex(D.data(), O.data(), Lv.data(), (int)D.size(), 1, p);
+        D.clear();
+        O.clear();
+        Lv.clear();
+        return r;
+    };
+    add_qkv(0, 0);
+    rc = make(&m->first);
+    for (int l = 0; l < cfg->n_layers && !rc; ++l) {
+        const qdq_llama_layer &w = layers[l];
+        // h += Wo att; gate, up from rmsnorm(h, ffn_norm); h += Wdown (silu(gate) * up)
+        D.push_back(desc(w.type[3], w.w[3], dim, dim, m->att, m->h));
+        O.push_back(opt(QDQ_X_PLAIN, QDQ_Y_ADD, nullptr, nullptr, 0.f, nullptr));
+        Lv.push_back(0);
+        D.push_back(desc(w.type[4], w.w[4], hid, dim, m->h, m->gate));
+        D.push_back(desc(w.type[5], w.w[5], hid, dim, m->h, m->up));
+        for (int i = 0; i < 2; ++i) {
+            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, w.ffn_norm, eps, nullptr));
+            Lv.push_back(1);
+        }
+        D.push_back(desc(w.type[6], w.w[6], dim, hid, m->gate, m->h));
+        O.push_back(opt(QDQ_X_SWIGLU, QDQ_Y_ADD, m->up, nullptr, 0.f, nullptr));
+        Lv.push_back(2);
+        if (l + 1 < cfg->n_layers) {
+            add_qkv(l + 1, 3);
+        } else {  // logits = Wout rmsnorm(h, output_norm), with their argmax
+            D.push_back(desc(output_type, output, cfg->vocab, dim, m->h, m->logits));
+            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, output_norm, eps, m->argmax));
+            Lv.push_back(3);
+        }
+        qdq_plan *p = nullptr;
+        rc = make(&p);
+        if (!rc) m->layer_plans.push_back(p);
+    }
+    if (rc) {
+        qdq_llama_destroy(m);
+        return rc;
+    }
+    *out = m;
+    return QDQ_OK;
+}
+
+int qdq_llama_forward(qdq_llama *m, int token, int pos, qdq_stream_t stream) {
+    if (m == nullptr) return QDQ_ERR_PTR;
+    if (token < 0 || token >= m->cfg.vocab || pos < 0 || pos >= m->cfg.max_seq) return QDQ_ERR_SHAPE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device) return QDQ_ERR_DEVICE;
+    const cudaStream_t s = (cudaStream_t)stream;
+    const qdq_llama_config &c = m->cfg;
+    const int D = c.dim / c.n_heads;
+    const int64_t kvl = (int64_t)c.max_seq * c.n_kv_heads * D;  // cache entries of one layer
+    // x = the token's embedding row, decoded
+    int rc = qdq_dequant_async(m->embd_type, (const char *)m->embd + (int64_t)token * m->embd_row_bytes, c.dim, m->h,
+                               stream);
+    if (!rc) rc = qdq_plan_run(m->first, stream);
+    for (int l = 0; l < c.n_layers && !rc; ++l) {
+        rc = launch_rope_attention(m->q, m->k, m->v, m->kcache + l * kvl, m->vcache + l * kvl, m->att, c.n_heads,
+                                   c.n_kv_heads, D, pos, c.rope_base, s);
+        if (!rc) rc = qdq_plan_run(m->layer_plans[l], stream);
+    }
+    return rc;
+}
+
+int qdq_llama_buffers(const qdq_llama *m, float **logits, int64_t **argmax, float **hidden, uint16_t **k_cache,
+                      uint16_t **v_cache) {
+    if (m == nullptr) return QDQ_ERR_PTR;
+    if (logits) *logits = m->logits;
+    if (argmax) *argmax = m->argmax;
+    if (hidden) *hidden = m->h;
+    if (k_cache) *k_cache = m->kcache;
+    if (v_cache) *v_cache = m->vcache;
+    return QDQ_OK;
+}
+
+int qdq_llama_launches(const qdq_llama *m) { return m ? 2 + 2 * m->cfg.n_layers : 0; }
+
+void qdq_llama_destroy(qdq_llama *m) {
+    if (m == nullptr) return;
+    if (m->first) qdq_plan_destroy(m->first);
+    for (qdq_plan *p : m->layer_plans) qdq_plan_destroy(p);
+    if (m->mem) cudaFree(m->mem);
+    delete m;
+}
+
+}  // extern "C"

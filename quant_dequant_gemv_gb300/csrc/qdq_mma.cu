@@ -138,7 +138,7 @@ struct MmaArgs {
 };
 
 struct Layout {
-    uint32_t x, x_stage, sums, bars, tmem_slot, total;
+    uint32_t x, x_stage, sums, xst, bars, tmem_slot, total;
 };
 
 // Q4_K group sums of x: a ring of kSumSlots sub-chunks, [slot][group 0..1][b_pad]
@@ -147,12 +147,25 @@ struct Layout {
 // so a slot is never refilled while its readers may still need it.
 constexpr int kSumSlots = 16;
 
+// fp32 x of a sub-chunk as it arrives from global memory: a ring of xstages(b_pad)
+// slots, batch row n at n * kXPitch (64 floats and 16 bytes of padding, so that
+// eight consecutive rows read 16 bytes each start in eight different bank groups).
+// The X warp copies sub-chunk j + xstages - 1 while it splits sub-chunk j, with
+// 16-byte asynchronous copies of its own lanes (they take the load path, not the
+// copy engine that streams W, so they do not queue behind the weight tiles).
+// At 16 padded columns (one item per lane) there is no ring: a lane's loads go
+// straight to registers, issued before the wait for the A stage, which measured
+// a few per cent faster there; from 32 columns the ring is faster.
+constexpr uint32_t kXPitch = 64 * 4 + 16;
+__host__ __device__ constexpr int xstages(int b_pad) { return b_pad >= 64 ? 2 : b_pad >= 32 ? 3 : 0; }
+
 __host__ __device__ inline Layout layout_for(uint32_t stage_bytes, int nraw, int nx, int b_pad) {
     Layout L;
     L.x = (uint32_t)nraw * stage_bytes;
     L.x_stage = (uint32_t)(256 * b_pad);  // four K-steps of 2 b_pad rows x 16 bf16
     L.sums = L.x + (uint32_t)nx * L.x_stage;  // nx = kAStages
-    L.bars = (L.sums + (uint32_t)(kSumSlots * 2 * b_pad * 4) + 127u) & ~127u;
+    L.xst = (L.sums + (uint32_t)(kSumSlots * 2 * b_pad * 4) + 127u) & ~127u;
+    L.bars = L.xst + (uint32_t)xstages(b_pad) * (uint32_t)b_pad * kXPitch;
     L.tmem_slot = L.bars + 8u * (6 * kMaxStages + 2 * kAStages + kSumSlots);
     L.total = L.tmem_slot + 16u;
     if (L.total < (uint32_t)kMinSmem) L.total = kMinSmem;
@@ -451,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t a_full = d_empty + 8 * kMaxStages, a_empty = a_full + 8 * kAStages;
     const uint32_t s_full = a_empty + 8 * kAStages;  // Q4_K group sums of a sub-chunk stored
     const uint32_t sums_a = sb + L.sums;
+    constexpr int kXs = xstages(BP);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nraw; ++s) {
@@ -533,42 +547,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nbytes) bulk_g2s_hint(dst, (const void *)src_al, nbytes, raw_full + 8 * s, pol);
         }
     } else if (warp == kWarpX) {
-        // ---- split X: for each sub-chunk, item (n, g) of a lane is batch row n and
-        // 32-column group g: eight float4 of x, split into bf16 hi + lo and stored
-        // in the canonical K-major layout of the X slot (x_hi rows 0..b_pad-1, x_lo
-        // rows b_pad..2 b_pad-1; rows past the batch are zero), plus (Q4_K) their
-        // sum. The loads of a lane's next item are in flight while it stores this one.
-        Ring rx(kAStages);
-        bool ok = true;
-        int j = 0;
-        constexpr int kItems = 2 * BP;
-        auto load_item = [&](int64_t c0, int ks, int it, float4 (&v)[8]) {
-            const int g = it / BP, n = it - g * BP;
-            const float *src = a.x + (int64_t)n * a.cols + c0 + 32 * g;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                v[i] = (n < a.batch && 2 * g + (i >> 2) < ks) ? __ldg(reinterpret_cast<const float4 *>(src) + i)
-                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        };
-        for (int u = u0; u < u1 && ok; ++u) {
-            const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
-            for (int sub = 0; sub < ns && ok; ++sub, ++j, rx.next()) {
-                const int s = rx.slot;
-                const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
-                const int64_t c0 = (int64_t)u * kUnitK + kSubK * sub;
-                float4 cur[8], nxt[8];
-                load_item(c0, ks, lane, cur);
+        // ---- split X. Sub-chunk j's fp32 x (64 columns of each batch row, fewer for
+        // a short last sub-chunk) comes from the staging ring (slot j mod kXs, filled
+        // kXs - 1 sub-chunks ahead) or, at 16 columns, straight from global memory.
+        // The split: item (n, g)
+        // of a lane is batch row n and 32-column group g, eight float4 split into
+        // bf16 hi + lo and stored in the canonical K-major layout of the X slot (x_hi
+        // rows 0..b_pad-1, x_lo rows b_pad..2 b_pad-1; rows past the batch are zero),
+        // plus (Q4_K) their sum.
+        if constexpr (kXs > 0) {
+            Ring rx(kAStages);
+            bool ok = true;
+            constexpr int kItems = 2 * BP;
+            const int nb = a.batch < BP ? a.batch : BP;
+            auto sub_ks = [&](int jj) { return jj == J - 1 ? ks_last : 4; };
+            // copy sub-chunk jj into its staging slot: 16 bytes per copy, lanes along a
+            // row; rows past the batch and columns past a short sub-chunk read as zero
+            auto issue = [&](int jj) {
+                const int slot = jj % kXs, ks = sub_ks(jj);
+                const int64_t c0 = (int64_t)(u0 + jj / (kUnitK / kSubK)) * kUnitK + kSubK * (jj % (kUnitK / kSubK));
+                const uint32_t dst0 = sb + L.xst + (uint32_t)(slot * BP) * kXPitch;
+    #pragma unroll 4
+                for (int i = lane; i < BP * 16; i += 32) {
+                    const int n = i >> 4, q = i & 15;
+                    const bool in = n < nb && q < 4 * ks;
+                    const float *src = a.x + (in ? (int64_t)n * a.cols + c0 + 4 * q : 0);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst0 + (uint32_t)n * kXPitch + 16u * q),
+                                 "l"(src), "r"(in ? 16 : 0)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            };
+            // sub-chunk j + kXs - 1 is copied once j has been handed to the MMA, into the
+            // slot that j - 1 used
+            int jn = 0, j = 0;  // next sub-chunk to copy, to split
+            for (; jn < kXs - 1 && jn < J; ++jn) issue(jn);
+            for (; j < J && ok; ++j, rx.next()) {
+                const int s = rx.slot, ks = sub_ks(j);
+                // sub-chunk j's group has landed when at most jn - j - 1 younger ones are pending
+                static_assert(xstages(32) <= 3 && xstages(64) <= 3, "wait_group counts below");
+                if (jn - j - 1 >= 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+                else asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();  // every lane's copies of the slot are visible to the warp
                 if (j >= kAStages) {
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_empty + 8 * s, rx.phase ^ 1, status));
                     if (!ok) break;
                 }
+                const uint32_t xst = sb + L.xst + (uint32_t)((j % kXs) * BP) * kXPitch;
                 const uint32_t xslot = sb + L.x + (uint32_t)s * L.x_stage;
                 const uint32_t sslot = sums_a + (uint32_t)((j % kSumSlots) * 2 * BP * 4);
-#pragma unroll 1
+    #pragma unroll 1
                 for (int it = lane; it < kItems; it += 32) {
-                    if (it + 32 < kItems) load_item(c0, ks, it + 32, nxt);
                     const int g = it / BP, n = it - g * BP;
-#pragma unroll
+                    float4 cur[8];
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        cur[i] = lds128f(xst + (uint32_t)n * kXPitch + 128u * g + 16u * i);
+    #pragma unroll
                     for (int h = 0; h < 4; ++h) {  // (K-step 2g + (h >> 1), 8-column half h & 1)
                         const int t = 2 * g + (h >> 1), kk = h & 1;
                         if (t < ks) {
@@ -584,13 +619,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if constexpr (TYPE == QDQ_Q4_K) {
                         float acc = 0.0f;
-#pragma unroll
+    #pragma unroll
                         for (int i = 0; i < 8; ++i) acc += (cur[i].x + cur[i].y) + (cur[i].z + cur[i].w);
                         asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (uint32_t)((g * BP + n) * 4)), "f"(acc)
                                      : "memory");
                     }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
                 }
                 // the MMA reads the X slot through the async proxy
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -599,9 +632,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (TYPE == QDQ_Q4_K) mbar_arrive(s_full + 8 * (j % kSumSlots));
                     mbar_arrive(a_full + 8 * s);
                 }
+                if (jn < J) issue(jn++);
             }
+            // copies still in flight after a failed wait land before the CTA exits
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncwarp();
+        } else {  // 16 columns: each lane loads its items straight into registers
+            Ring rx(kAStages);
+            bool ok = true;
+            int j = 0;
+            constexpr int kItems = 2 * BP;
+            auto load_item = [&](int64_t c0, int ks, int it, float4 (&v)[8]) {
+                const int g = it / BP, n = it - g * BP;
+                const float *src = a.x + (int64_t)n * a.cols + c0 + 32 * g;
+    #pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[i] = (n < a.batch && 2 * g + (i >> 2) < ks) ? __ldg(reinterpret_cast<const float4 *>(src) + i)
+                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            };
+            for (int u = u0; u < u1 && ok; ++u) {
+                const int uk = unit_k(a, u), ns = (uk + kSubK - 1) / kSubK;
+                for (int sub = 0; sub < ns && ok; ++sub, ++j, rx.next()) {
+                    const int s = rx.slot;
+                    const int ks = (uk - kSubK * sub) >= kSubK ? 4 : (uk - kSubK * sub) / 16;
+                    const int64_t c0 = (int64_t)u * kUnitK + kSubK * sub;
+                    float4 cur[8], nxt[8];
+                    load_item(c0, ks, lane, cur);
+                    if (j >= kAStages) {
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_empty + 8 * s, rx.phase ^ 1, status));
+                        if (!ok) break;
+                    }
+                    const uint32_t xslot = sb + L.x + (uint32_t)s * L.x_stage;
+                    const uint32_t sslot = sums_a + (uint32_t)((j % kSumSlots) * 2 * BP * 4);
+    #pragma unroll 1
+                    for (int it = lane; it < kItems; it += 32) {
+                        if (it + 32 < kItems) load_item(c0, ks, it + 32, nxt);
+                        const int g = it / BP, n = it - g * BP;
+    #pragma unroll
+                        for (int h = 0; h < 4; ++h) {  // (K-step 2g + (h >> 1), 8-column half h & 1)
+                            const int t = 2 * g + (h >> 1), kk = h & 1;
+                            if (t < ks) {
+                                uint32_t hi[4], lo[4];
+                                split_pair(pack2(cur[2 * h].x, cur[2 * h].y), hi[0], lo[0]);
+                                split_pair(pack2(cur[2 * h].z, cur[2 * h].w), hi[1], lo[1]);
+                                split_pair(pack2(cur[2 * h + 1].x, cur[2 * h + 1].y), hi[2], lo[2]);
+                                split_pair(pack2(cur[2 * h + 1].z, cur[2 * h + 1].w), hi[3], lo[3]);
+                                const uint32_t blk = xslot + (uint32_t)(t * 64 * BP + kk * 128 + (n & 7) * 16);
+                                sts128(blk + (uint32_t)((n >> 3) * 256), hi);
+                                sts128(blk + (uint32_t)(((BP + n) >> 3) * 256), lo);
+                            }
+                        }
+                        if constexpr (TYPE == QDQ_Q4_K) {
+                            float acc = 0.0f;
+    #pragma unroll
+                            for (int i = 0; i < 8; ++i) acc += (cur[i].x + cur[i].y) + (cur[i].z + cur[i].w);
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (uint32_t)((g * BP + n) * 4)), "f"(acc)
+                                         : "memory");
+                        }
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+                    }
+                    // the MMA reads the X slot through the async proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (TYPE == QDQ_Q4_K) mbar_arrive(s_full + 8 * (j % kSumSlots));
+                        mbar_arrive(a_full + 8 * s);
+                    }
+                }
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else if (warp == kWarpMma) {
         // ---- MMA issue: the whole warp runs the loop with warp-uniform operands and
         // one elected lane issues a sub-chunk's MMAs in one go, so the descriptors

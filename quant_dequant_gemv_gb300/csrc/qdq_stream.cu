@@ -40,8 +40,8 @@ static unsigned long long *s_trace = nullptr;
 #endif
 
 template <int MAXD, int MAXL>
-static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, const int *level, int n, int batch,
-                      unsigned *counters) {
+static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, const qdq_gemv_opts *opts,
+                      const int *level, int n, int batch, unsigned *counters, unsigned long long *amax_slot) {
     memset(A, 0, sizeof(*A));
 #ifdef QDQ_TRACE
     A->trace = s_trace;
@@ -66,6 +66,19 @@ static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, con
         d.cols = (int32_t)descs[i].cols;
         d.type = descs[i].type;
         d.rb = (int32_t)((descs[i].cols / blk_weights(d.type)) * blk_bytes(d.type));
+        if (opts) {
+            d.xop = opts[i].x_op;
+            d.yop = opts[i].y_op;
+            d.x2 = opts[i].x2;
+            d.nw = opts[i].norm_w;
+            d.eps = opts[i].eps;
+            if (opts[i].argmax) {
+                d.amax = 1;
+                A->amax_slot = amax_slot;
+                A->amax_y = descs[i].y;
+                A->amax_out = (long long *)opts[i].argmax;
+            }
+        }
     }
     // staged copy kinds per (level, x)
     for (int lv = 0; lv < A->nlevels; ++lv) {
@@ -80,8 +93,8 @@ static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, con
 
 static int bt_of(int batch) { return batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8; }
 
-int stream_plan_build(const qdq_gemv_desc *descs, const int *level, int n, int batch, unsigned *counters,
-                      int sm_count, StreamPlanHost **out) {
+int stream_plan_build(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n, int batch,
+                      unsigned *counters, unsigned long long *amax_slot, int sm_count, StreamPlanHost **out) {
     StreamPlanHost *p = new (std::nothrow) StreamPlanHost();
     if (!p) return QDQ_ERR_CUDA;
     p->bt = bt_of(batch);
@@ -93,14 +106,14 @@ int stream_plan_build(const qdq_gemv_desc *descs, const int *level, int n, int b
         using A = StreamArgs<kMaxPlanDescs, kMaxPlanLevels>;
         A *args = (A *)malloc(sizeof(A));
         if (!args) { delete p; return QDQ_ERR_CUDA; }
-        fill_args(args, descs, level, n, batch, counters);
+        fill_args(args, descs, opts, level, n, batch, counters, amax_slot);
         p->args = args;
         p->args_bytes = sizeof(A);
     } else {
         using A = StreamArgs<kMaxGroupDescs, 1>;
         A *args = (A *)malloc(sizeof(A));
         if (!args) { delete p; return QDQ_ERR_CUDA; }
-        fill_args(args, descs, level, n, batch, counters);
+        fill_args(args, descs, opts, level, n, batch, counters, amax_slot);
         p->args = args;
         p->args_bytes = sizeof(A);
     }
@@ -125,7 +138,7 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
     p.cooperative = true;
     p.args = &args;
     p.args_bytes = sizeof(A);
-    fill_args(&args, descs, level, n, batch, counters);
+    fill_args(&args, descs, nullptr, level, n, batch, counters, nullptr);
     return stream_plan_launch(&p, stream);
 }
 

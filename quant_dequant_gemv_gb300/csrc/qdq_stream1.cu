@@ -108,7 +108,8 @@ struct Smem {
     static constexpr int kRanges = kDstStride + Cfg<BT>::kBufRows * 4;
     static constexpr int kRing = kRanges + 2 * MAXD * 8;              // producer: live tiles' ring ranges
     static constexpr int kBars = kRing + 2 * kSlots * 4;
-    static constexpr int kBytes = kBars + (2 * kSlots + 2) * 8;
+    static constexpr int kRed = kBars + (2 * kSlots + 2) * 8;          // per-warp partial sums of x^2 [warp][b]
+    static constexpr int kBytes = kRed + 16 * 8 * 4;
 };
 template <int BT, int MAXD>
 constexpr bool smem_aligned() {
@@ -368,9 +369,61 @@ QDQ_DEV int xunit(int u) { return (u & ~15) | ((u & 15) ^ ((u >> 3) & 6)); }
 // (k * BT + b) * 2048 + w * 256 (swizzled units). The consumer warps stage
 // (chunk, slice) pairs in turn: warp cw takes pairs cw, cw + ncw, ...
 // ---------------------------------------------------------------------------
+// rmsnorm of the GEMV input ("S21 The Capstone: picoLM, in Python", section 4:
+// rmsnorm(xb, x, weight, dim) before the q/k/v and gate/up projections): inv[b] =
+// 1 / sqrt(mean over the cols entries of x_b^2 + eps) for each batch column. The
+// consumer warps sum strided float4 of the whole of x (not only the staged
+// window), then every thread adds the warps' sums in warp order, so every
+// thread holds the same inv.
+template <int BT>
+QDQ_DEV void rms_scale(const DevDesc &d, int batch, int cw, int ncw, int lane, float *red, float (&inv)[BT]) {
+    float ss[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) ss[b] = 0.f;
+    for (int c = 4 * (cw * 32 + lane); c < d.cols; c += 4 * 32 * ncw) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b)
+            if (b < batch) {
+                const float4 v = __ldcg((const float4 *)(d.x + (int64_t)b * d.cols + c));
+                ss[b] += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+            }
+    }
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss[b] += __shfl_xor_sync(0xFFFFFFFFu, ss[b], o);
+        if (lane == 0) red[cw * 8 + b] = ss[b];
+    }
+    named_bar_sync(kFlushBar, ncw * 32);
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        float t = 0.f;
+        for (int w = 0; w < ncw; ++w) t += red[w * 8 + b];
+        inv[b] = 1.0f / sqrtf(t / (float)d.cols + d.eps);
+    }
+}
+
+QDQ_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// The value the dot product reads at x[b][col..col+3] (QDQ_X_*): as stored,
+// rmsnorm-scaled, or silu(gate) * up.
+template <int BT>
+QDQ_DEV float4 x_in(const DevDesc &d, int b, int col, int off, const float (&inv)[BT], float4 v) {
+    if (d.xop == QDQ_X_RMSNORM) {
+        const float4 w = __ldg((const float4 *)(d.nw + col + off));
+        const float s = inv[b];
+        return make_float4(v.x * s * w.x, v.y * s * w.y, v.z * s * w.z, v.w * s * w.w);
+    }
+    if (d.xop == QDQ_X_SWIGLU) {
+        const float4 u = __ldcg((const float4 *)(d.x2 + (int64_t)b * d.cols + col + off));
+        return make_float4(silu(v.x) * u.x, silu(v.y) * u.y, silu(v.z) * u.z, silu(v.w) * u.w);
+    }
+    return v;
+}
+
 template <int BT>
 QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, int cw, int ncw, int lane,
-                      float *xbuf) {
+                      const float (&inv)[BT], float *xbuf) {
     const int nk = nkinds(kinds), stride = xfloats_per_chunk<BT>(kinds);
     const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
     for (int i = cw; i < (w1 - w0) * kSlicesPerChunk; i += ncw) {
@@ -381,8 +434,9 @@ QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, in
         for (int b = 0; b < BT; ++b) {
             const bool ok = b < batch && col < d.cols;
             const float *xr = d.x + (int64_t)b * d.cols + col;
-            const float4 a = ok ? __ldcg((const float4 *)xr) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 c = ok ? __ldcg((const float4 *)(xr + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 a = ok ? x_in<BT>(d, b, col, 0, inv, __ldcg((const float4 *)xr)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 c =
+                ok ? x_in<BT>(d, b, col, 4, inv, __ldcg((const float4 *)(xr + 4))) : make_float4(0.f, 0.f, 0.f, 0.f);
             int slot = 0;
             if (kinds & 1) {
                 float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
@@ -808,6 +862,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
     uint64_t *dst = (uint64_t *)(smem + SM::kDst);
     int *dstride = (int *)(smem + SM::kDstStride);
     int64_t *ranges = (int64_t *)(smem + SM::kRanges);
+    float *red = (float *)(smem + SM::kRed);
     const uint32_t ring_a = smem_u32(smem);
     const uint32_t full_a = smem_u32(smem + SM::kBars), empty_a = full_a + 8 * kSlots;
 
@@ -889,16 +944,33 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
 
     // Adds the eight warps' partials of every buffered row (warp order) and stores
     // y (adding to it for rows whose earlier columns were stored before).
+    // dst[i]: y address of buffer row i; bit 0: add to what y holds (a later
+    // column window, or QDQ_Y_ADD), bit 1: the row takes part in the argmax.
     auto flush = [&]() {
         named_bar_sync(kFlushBar, kCW * 32);  // partials and addresses are in place
+        unsigned long long best = 0ull;  // argmax candidate: (ordered value, ~row) packed
         for (int i = ctid; BT == 1 && i < buf_rows; i += kCW * 32) {
             float sum = 0.f;
 #pragma unroll
             for (int w = 0; w < kCW; ++w) sum += part[w * kBufRows + i];
             const uint64_t d = dst[i];
-            float *yp = (float *)(uintptr_t)(d & ~(uint64_t)1);
+            float *yp = (float *)(uintptr_t)(d & ~(uint64_t)3);
             if (d & 1) sum += __ldcg(yp);
             *yp = sum;
+            if (d & 2) {
+                const unsigned u = __float_as_uint(sum), key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                const unsigned row = (unsigned)(yp - a.amax_y);
+                const unsigned long long k = ((unsigned long long)key << 32) | (0xFFFFFFFFu - row);
+                best = k > best ? k : best;
+            }
+        }
+        if (BT == 1 && a.amax_slot != nullptr) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                best = other > best ? other : best;
+            }
+            if (lane == 0 && best != 0ull) atomicMax(&a.amax_slot[0], best);
         }
         // batch columns: entry i of a warp's column is (row i / BT, column i % BT)
         for (int i = ctid; BT > 1 && i < buf_rows * BT; i += kCW * 32) {
@@ -908,7 +980,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
 #pragma unroll
             for (int w = 0; w < kCW; ++w) sum += part[w * kBufRows * BT + i];
             const uint64_t d = dst[row];
-            float *yp = (float *)(uintptr_t)(d & ~(uint64_t)1) + (int64_t)b * dstride[row];
+            float *yp = (float *)(uintptr_t)(d & ~(uint64_t)3) + (int64_t)b * dstride[row];
             if (d & 1) sum += __ldcg(yp);
             *yp = sum;
         }
@@ -942,7 +1014,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 // the buffer is shared: a later x of the same level waits for every
                 // warp to be done with it; then every warp stages its slices
                 if (level_staged) named_bar_sync(kFlushBar, kCW * 32);
-                stage_xb<BT>(d, tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, xbuf);
+                float inv[BT];
+#pragma unroll
+                for (int b = 0; b < BT; ++b) inv[b] = 1.f;
+                if (d.xop == QDQ_X_RMSNORM) rms_scale<BT>(d, a.batch, cw, kCW, lane, red, inv);
+                stage_xb<BT>(d, tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf);
                 named_bar_sync(kFlushBar, kCW * 32);
                 level_staged = true;
             }
@@ -953,7 +1029,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 buf_rows += tl.nrows;
                 if (cw == 0)
                     for (int i = lane; i < tl.nrows; i += 32)
-                        dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) | (tl.first_win ? 0u : 1u),
+                        dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) |
+                                           ((tl.first_win && d.yop == QDQ_Y_STORE) ? 0u : 1u) | (d.amax ? 2u : 0u),
                         dstride[rg_base + i] = (int)d.rows;
                 if constexpr (BT == 1) {  // batch 1 adds every unit into the warp's column
                     for (int i = lane; i < tl.nrows; i += 32) mypart[rg_base + i] = 0.f;
@@ -1025,6 +1102,20 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
             had_tiles = false;
             dep_pending = false;  // a level without tiles here waits for nothing
         });
+    // The argmax: every CTA's candidates are in the slot once it has arrived; the
+    // last CTA to arrive writes the winning row and clears the slot for the next
+    // run. (The flush that issued this CTA's candidates ended with a barrier of
+    // the consumer warps, and the fence orders them before the arrival.)
+    if (a.amax_slot != nullptr && cw == 0 && lane == 0) {
+        __threadfence();
+        if (atomicAdd(&a.amax_slot[1], 1ull) == (unsigned long long)(P - 1)) {
+            const unsigned long long v = atomicAdd(&a.amax_slot[0], 0ull);
+            *a.amax_out = (long long)(0xFFFFFFFFull - (v & 0xFFFFFFFFull));
+            a.amax_slot[0] = 0ull;
+            a.amax_slot[1] = 0ull;
+            __threadfence();
+        }
+    }
 }
 
 }  // namespace s1

@@ -23,6 +23,13 @@ struct DevDesc {
     int32_t pad0;   // keeps the fields below at the offsets the kernel's register allocation was tuned with
     int32_t kinds;  // bit k: the level's x needs swizzled copy kind k (0 plain, 2 q4_0-scaled)
     int32_t pad1;
+    // step glue fused into the GEMV (plans only; zero elsewhere): the x the
+    // dot product reads (QDQ_X_*), how y is written (QDQ_Y_*), and whether the
+    // rows take part in the plan's argmax
+    const float *x2;  // QDQ_X_SWIGLU: the up input
+    const float *nw;  // QDQ_X_RMSNORM: the norm weights
+    float eps;
+    int32_t xop, yop, amax;
 };
 
 template <int MAXD, int MAXL>
@@ -30,6 +37,12 @@ struct StreamArgs {
     int32_t ndesc, nlevels, batch, pad;
     unsigned *counters;
     unsigned long long *trace;  // QDQ_TRACE builds only: per-CTA phase timestamps
+    // argmax over the y of the GEMV with amax set (batch 1): packed running
+    // maximum and CTA arrivals (plan-owned, zero between runs), the y base its
+    // row indices count from, and where the winning index goes
+    unsigned long long *amax_slot;
+    const float *amax_y;
+    long long *amax_out;
     int32_t level_start[MAXL + 1];
     DevDesc d[MAXD];
 };

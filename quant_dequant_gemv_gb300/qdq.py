@@ -32,6 +32,28 @@ class GemvDesc(ctypes.Structure):
                 ("cols", _I64), ("x", _P), ("y", _P)]
 
 
+# qdq_gemv_opts: step glue fused into a plan's GEMV
+X_PLAIN, X_RMSNORM, X_SWIGLU = 0, 1, 2
+Y_STORE, Y_ADD = 0, 1
+
+
+class GemvOpts(ctypes.Structure):
+    _fields_ = [("x_op", ctypes.c_int32), ("y_op", ctypes.c_int32), ("x2", _P), ("norm_w", _P),
+                ("eps", ctypes.c_float), ("reserved", ctypes.c_int32), ("argmax", _P)]
+
+
+class LlamaConfig(ctypes.Structure):
+    _fields_ = [("dim", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_layers", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("vocab", ctypes.c_int32),
+                ("max_seq", ctypes.c_int32), ("reserved", ctypes.c_int32), ("rope_base", ctypes.c_float),
+                ("norm_eps", ctypes.c_float)]
+
+
+class LlamaLayer(ctypes.Structure):
+    _fields_ = [("w", _P * 7), ("type", ctypes.c_int32 * 7), ("reserved", ctypes.c_int32),
+                ("attn_norm", _P), ("ffn_norm", _P)]
+
+
 def lib() -> ctypes.CDLL:
     """Load libqdq.so (built by __graft_entry__.build()). Raises if it is absent."""
     global _lib
@@ -51,6 +73,8 @@ def lib() -> ctypes.CDLL:
             "qdq_gemv_group": (_INT, [ctypes.POINTER(GemvDesc), _INT, _INT, _P]),
             "qdq_plan_create": (_INT, [ctypes.POINTER(GemvDesc), ctypes.POINTER(_INT), _INT, _INT,
                                        ctypes.POINTER(_P)]),
+            "qdq_plan_create_ex": (_INT, [ctypes.POINTER(GemvDesc), ctypes.POINTER(GemvOpts),
+                                          ctypes.POINTER(_INT), _INT, _INT, ctypes.POINTER(_P)]),
             "qdq_plan_run": (_INT, [_P, _P]),
             "qdq_plan_run_io": (_INT, [_P, _P, _P, _P, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
             "qdq_plan_reset": (_INT, [_P, _P]),
@@ -59,6 +83,15 @@ def lib() -> ctypes.CDLL:
             "qdq_get_device_status": (_INT, [_P]),
             "qdq_selftest_wait_timeout": (_INT, [_I64, _P]),
             "qdq_gemv_levels_noalloc": (_INT, [ctypes.POINTER(GemvDesc), ctypes.POINTER(_INT), _INT, _INT, _P]),
+            "qdq_rope_attention": (_INT, [_P, _P, _P, _P, _P, _P, _INT, _INT, _INT, _INT, _INT, ctypes.c_float,
+                                          _P]),
+            "qdq_llama_create": (_INT, [ctypes.POINTER(LlamaConfig), _P, _INT, ctypes.POINTER(LlamaLayer), _P, _P,
+                                        _INT, ctypes.POINTER(_P)]),
+            "qdq_llama_forward": (_INT, [_P, _INT, _INT, _P]),
+            "qdq_llama_buffers": (_INT, [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                                         ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+            "qdq_llama_launches": (_INT, [_P]),
+            "qdq_llama_destroy": (None, [_P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -71,9 +104,11 @@ def lib() -> ctypes.CDLL:
 # Every name the header declares (the C ABI's exported symbols).
 EXPORTS = ["qdq_block_bytes", "qdq_block_weights", "qdq_status_string", "qdq_device_sm_count",
            "qdq_dequant", "qdq_dequant_async", "qdq_gemv", "qdq_gemv_group", "qdq_plan_create",
+           "qdq_plan_create_ex",
            "qdq_plan_run", "qdq_plan_run_io", "qdq_plan_reset", "qdq_plan_destroy",
            "qdq_plan_launches", "qdq_get_device_status", "qdq_selftest_wait_timeout",
-           "qdq_gemv_levels_noalloc"]
+           "qdq_gemv_levels_noalloc", "qdq_rope_attention", "qdq_llama_create", "qdq_llama_forward",
+           "qdq_llama_buffers", "qdq_llama_launches", "qdq_llama_destroy"]
 
 
 def _ptr(t) -> int:
@@ -140,12 +175,23 @@ def gemv_group(items: Sequence[tuple], batch: int = 1, stream=None) -> None:
 class Plan:
     """A decode step's GEMVs in dependency levels, run as one persistent launch."""
 
-    def __init__(self, items: Sequence[tuple], levels: Sequence[int], batch: int = 1):
-        self._keep = items  # the caller's buffers must outlive the plan
+    def __init__(self, items: Sequence[tuple], levels: Sequence[int], batch: int = 1,
+                 opts: Sequence[dict | None] | None = None):
+        """opts[i] (optional): dict with x_op, y_op, x2, norm_w, eps, argmax for items[i]."""
+        self._keep = (items, opts)  # the caller's buffers must outlive the plan
         self.batch = batch
         lv = (_INT * len(levels))(*levels)
         h = _P()
-        _check(lib().qdq_plan_create(_descs(items), lv, len(items), batch, ctypes.byref(h)), "qdq_plan_create")
+        if opts is None:
+            _check(lib().qdq_plan_create(_descs(items), lv, len(items), batch, ctypes.byref(h)), "qdq_plan_create")
+        else:
+            oa = (GemvOpts * max(len(items), 1))()
+            for i, o in enumerate(opts):
+                o = o or {}
+                oa[i] = GemvOpts(o.get("x_op", X_PLAIN), o.get("y_op", Y_STORE), _ptr(o.get("x2")),
+                                 _ptr(o.get("norm_w")), float(o.get("eps", 0.0)), 0, _ptr(o.get("argmax")))
+            _check(lib().qdq_plan_create_ex(_descs(items), oa, lv, len(items), batch, ctypes.byref(h)),
+                   "qdq_plan_create_ex")
         self._h = h
 
     def run(self, stream=None) -> None:
@@ -190,3 +236,77 @@ def get_device_status(stream=None) -> int:
 
 def selftest_wait_timeout(timeout_ns: int, stream=None) -> None:
     _check(lib().qdq_selftest_wait_timeout(timeout_ns, _stream(stream)), "qdq_selftest_wait_timeout")
+
+
+def rope_attention(q, k, v, k_cache, v_cache, out, n_heads: int, n_kv_heads: int, head_dim: int, pos: int,
+                   max_seq: int, rope_base: float = 10000.0, stream=None) -> None:
+    """RoPE, fp16 cache append at `pos` and GQA attention of one position (qdq_rope_attention)."""
+    _check(lib().qdq_rope_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(out), n_heads,
+                                    n_kv_heads, head_dim, pos, max_seq, rope_base, _stream(stream)),
+           "qdq_rope_attention")
+
+
+class _DeviceArray:
+    """__cuda_array_interface__ over a library-owned device buffer (no copy)."""
+
+    def __init__(self, ptr: int, shape: tuple, typestr: str):
+        self.__cuda_array_interface__ = {"shape": shape, "typestr": typestr, "data": (ptr, False), "version": 2,
+                                         "strides": None}
+
+
+def device_view(ptr: int, shape: tuple, typestr: str):
+    """A torch tensor viewing `ptr` (device memory the library owns)."""
+    import torch
+    return torch.as_tensor(_DeviceArray(ptr, shape, typestr), device="cuda")
+
+
+class Llama:
+    """One-token forward passes of a Llama-architecture model (qdq_llama_*).
+
+    embd, output: (type, W) of the token embedding and output matrices;
+    layers: per layer a dict of q k v o gate up down -> (type, W) and attn_norm,
+    ffn_norm -> fp32 tensors; output_norm: fp32 tensor. The tensors must outlive
+    the model."""
+
+    def __init__(self, dim, hidden, n_layers, n_heads, n_kv_heads, vocab, max_seq, embd, layers, output_norm,
+                 output, rope_base=10000.0, norm_eps=1e-5):
+        self._keep = (embd, layers, output_norm, output)
+        self.cfg = LlamaConfig(dim, hidden, n_layers, n_heads, n_kv_heads, vocab, max_seq, 0, rope_base, norm_eps)
+        arr = (LlamaLayer * n_layers)()
+        for i, lw in enumerate(layers):
+            for j, name in enumerate(("q", "k", "v", "o", "gate", "up", "down")):
+                t, W = lw[name]
+                arr[i].w[j] = _ptr(W)
+                arr[i].type[j] = t
+            arr[i].attn_norm = _ptr(lw["attn_norm"])
+            arr[i].ffn_norm = _ptr(lw["ffn_norm"])
+        h = _P()
+        _check(lib().qdq_llama_create(ctypes.byref(self.cfg), _ptr(embd[1]), embd[0], arr, _ptr(output_norm),
+                                      _ptr(output[1]), output[0], ctypes.byref(h)), "qdq_llama_create")
+        self._h = h
+        ptrs = [_P() for _ in range(5)]
+        _check(lib().qdq_llama_buffers(h, *[ctypes.byref(p) for p in ptrs]), "qdq_llama_buffers")
+        kv = n_kv_heads * (dim // n_heads)
+        self.logits = device_view(ptrs[0].value, (vocab,), "<f4")
+        self.argmax = device_view(ptrs[1].value, (1,), "<i8")
+        self.hidden = device_view(ptrs[2].value, (dim,), "<f4")
+        self.k_cache = device_view(ptrs[3].value, (n_layers, max_seq, kv), "<f2")
+        self.v_cache = device_view(ptrs[4].value, (n_layers, max_seq, kv), "<f2")
+
+    def forward(self, token: int, pos: int, stream=None) -> None:
+        _check(lib().qdq_llama_forward(self._h, token, pos, _stream(stream)), "qdq_llama_forward")
+
+    @property
+    def launches(self) -> int:
+        return lib().qdq_llama_launches(self._h)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().qdq_llama_destroy(self._h)
+            self._h = _P()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -202,8 +202,12 @@ def llama_shapes(dim: int, hidden: int, n_heads: int, n_kv_heads: int) -> dict:
 
 
 def gen_llama_model(dim: int, hidden: int, n_layers: int, n_heads: int, n_kv_heads: int, vocab: int,
-                    seed: int, embd_type: int = Q4_K, out_type: int = Q6_K) -> dict:
-    """Raw blocks of every tensor and the fp32 norm vectors, from one seed."""
+                    seed: int, embd_type: int = Q4_K, out_type: int = Q6_K, norm_scale: float = 1.0) -> dict:
+    """Raw blocks of every tensor and the fp32 norm vectors (times norm_scale), from one seed.
+
+    With the workload's block draws a weight is of order 1, so q.k scores reach
+    thousands and the softmax is one-hot; a norm_scale of about 0.02 keeps the
+    scores of order 1 (every position then weighs in)."""
     rng = np.random.default_rng(seed)
     shapes = llama_shapes(dim, hidden, n_heads, n_kv_heads)
     m = {"token_embd": (embd_type, vocab, dim, gen_blocks(embd_type, vocab * dim // BLOCK_WEIGHTS[embd_type], rng)),
@@ -214,9 +218,9 @@ def gen_llama_model(dim: int, hidden: int, n_layers: int, n_heads: int, n_kv_hea
             r, c = shapes[name]
             t = LAYER_TYPES[name]
             lw[name] = (t, r, c, gen_blocks(t, r * c // BLOCK_WEIGHTS[t], rng))
-        lw["attn_norm"] = rng.uniform(0.5, 1.5, dim).astype(np.float32)
-        lw["ffn_norm"] = rng.uniform(0.5, 1.5, dim).astype(np.float32)
+        lw["attn_norm"] = (norm_scale * rng.uniform(0.5, 1.5, dim)).astype(np.float32)
+        lw["ffn_norm"] = (norm_scale * rng.uniform(0.5, 1.5, dim)).astype(np.float32)
         m["layers"].append(lw)
-    m["output_norm"] = rng.uniform(0.5, 1.5, dim).astype(np.float32)
+    m["output_norm"] = (norm_scale * rng.uniform(0.5, 1.5, dim)).astype(np.float32)
     m["output"] = (out_type, vocab, dim, gen_blocks(out_type, vocab * dim // BLOCK_WEIGHTS[out_type], rng))
     return m
