@@ -47,6 +47,9 @@ WORKLOADS = {
     "ffn_q6k": "Q6_K GEMV 2048x5632 (ffn_down shape)",
     "q8_0": "PETIT q8_0 GEMVs 14336x4096 and 4096x14336",
     "q4_0": "PETIT q4_0 GEMVs 14336x4096 and 4096x14336",
+    "token": "1.1B Llama-shape token step, batch 1, greedy decode: embedding row, 22 layers of rmsnorm -> "
+             "q/k/v -> RoPE + fp16 KV cache + GQA attention -> o + residual -> rmsnorm -> gate/up -> SwiGLU -> "
+             "down + residual, final rmsnorm -> output head + argmax (Q4_K_M mix, 667,152,384 GEMV weight bytes)",
     "dequant_q4k": "standalone dequantisation, Q4_K, 2^27 weights -> fp32",
     "dequant_q6k": "standalone dequantisation, Q6_K, 2^27 weights -> fp32",
     "dequant_q8_0": "standalone dequantisation, PETIT q8_0, 2^27 weights -> fp32",
@@ -58,6 +61,8 @@ DEQUANT_N = 1 << 27  # weights per dequantisation step: in + out bytes are sever
 
 
 def workload_levels(name: str, layers: int = 22) -> list[list[synth.Gemv]]:
+    if name == "token":
+        return synth.llama_1b_step(layers)
     if name in DEQUANT_TYPES:
         return []
     if name == "step":
@@ -291,6 +296,88 @@ def dequant_cpu_baseline(workload: str, budget_s: float = 8.0) -> dict:
     return {"value": round(reps * dequant_bytes(qtype, n) / spent / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle", **host_cpu(),
             "sample": f"{reps} dequantisations of 2^22 weights ({spent:.1f} s), plain C oracle, one thread"}
+
+
+TOKEN_POS0 = 64  # the timed token steps start at this cache position (earlier rows filled in warm-up)
+
+
+def token_bytes(layers: int, pos: int) -> int:
+    """Algorithmic bytes of one token step at cache position pos: every GEMV's
+    weights, the embedding row, the fp16 key/value rows read (positions 0..pos of
+    every layer), the norm vectors, and the activation vectors each level reads
+    and writes once."""
+    L = synth.LLAMA_1B
+    dim, hid, kv, vocab = L["hidden"], L["ffn"], L["n_kv_heads"] * L["head_dim"], L["vocab"]
+    w = synth.step_weight_bytes(synth.llama_1b_step(layers))
+    embd = synth.row_bytes(synth.Q4_K, dim)
+    cache = layers * 2 * (pos + 1) * kv * 2
+    norms = (2 * layers + 1) * dim * 4
+    act = layers * 4 * (3 * dim + 2 * kv + 3 * hid + dim + dim) + 4 * (dim + vocab)
+    return w + embd + cache + norms + act
+
+
+def run_token(args, device):
+    """Greedy decoding through qdq_llama_forward: each timed step is one token at
+    the next cache position; the token fed is the previous step's argmax."""
+    import torch
+    from quant_dequant_gemv_gb300 import build, qdq
+
+    build.build()
+    L = synth.LLAMA_1B
+    cfg = dict(dim=L["hidden"], hidden=L["ffn"], n_layers=args.layers, n_heads=L["n_heads"],
+               n_kv_heads=L["n_kv_heads"], vocab=L["vocab"])
+    m = synth.gen_llama_model(seed=0, **cfg)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    layers = []
+    for lw in m["layers"]:
+        d = {name: (lw[name][0], t(lw[name][3])) for name in synth.LAYER_TENSORS}
+        d["attn_norm"], d["ffn_norm"] = t(lw["attn_norm"]), t(lw["ffn_norm"])
+        layers.append(d)
+    e, o = m["token_embd"], m["output"]
+    max_seq = TOKEN_POS0 + 2 * (args.steps + args.warmup) + 8
+    model = qdq.Llama(max_seq=max_seq, embd=(e[0], t(e[3])), layers=layers, output_norm=t(m["output_norm"]),
+                      output=(o[0], t(o[3])), **cfg)
+    stream = torch.cuda.current_stream(device)
+    pos = 0
+    while pos < TOKEN_POS0 + args.warmup:  # fill the cache up to the timed positions
+        model.forward(pos % cfg["vocab"], pos, stream)
+        pos += 1
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0 = pos
+    t0.record(stream)
+    for i, ev in enumerate(evs):
+        ev[0].record(stream)
+        model.forward(int(i * 7919 % cfg["vocab"]), p0 + i, stream)
+        ev[1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    rc = qdq.get_device_status(stream)
+    if rc != 0:
+        raise SystemExit(f"device status after timing: {qdq.status_string(rc)}")
+    # end to end: greedy decoding, the argmax read back to the host each step
+    # and fed as the next token
+    am = torch.empty(1, dtype=torch.int64).pin_memory()
+    pos = p0 + K
+    tok = 1
+    E = K
+    te = time.perf_counter()
+    for i in range(E):
+        model.forward(tok, pos + i, stream)
+        am.copy_(model.argmax, non_blocking=True)
+        stream.synchronize()
+        tok = int(am.item())
+    e2e_s = (time.perf_counter() - te) / E
+    launches = model.launches
+    abytes = token_bytes(args.layers, p0 + K // 2)
+    model.close()
+    return {"total_ms": t0.elapsed_time(t1), "launch_ms": [a.elapsed_time(b) for a, b in evs], "abytes": abytes,
+            "clocks": clocks, "e2e_s": e2e_s, "h2d": 0, "d2h": 8, "launches": K * launches}
 
 
 def run_ours(args, rank, world, device):
@@ -577,6 +664,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     levels = workload_levels(args.workload, args.layers)
     abytes = (dequant_bytes(DEQUANT_TYPES[args.workload], DEQUANT_N) if args.workload in DEQUANT_TYPES
+              else token_bytes(args.layers, TOKEN_POS0 + args.warmup + args.steps // 2) if args.workload == "token"
               else algorithmic_bytes(levels, args.batch))
     step_bytes = abytes
     wname = WORKLOADS[args.workload]
@@ -632,7 +720,10 @@ def main():
         dist.init_process_group("nccl")
     device = torch.device(f"cuda:{local}")
     torch.cuda.set_device(device)
-    r = run_dequant(args, device) if args.workload in DEQUANT_TYPES else run_ours(args, rank, world, device)
+    if args.workload == "token" and args.batch != 1:
+        raise SystemExit("the token workload is batch 1")
+    r = (run_dequant(args, device) if args.workload in DEQUANT_TYPES
+         else run_token(args, device) if args.workload == "token" else run_ours(args, rank, world, device))
 
     total_ms, e2e_s = slowest_replica(r["total_ms"], r["e2e_s"], world, device)
     ms_step = total_ms / args.steps
@@ -657,7 +748,8 @@ def main():
             "tok_s": round(world * 1e3 / ms_step, 1),
             "config": {"workload": wname, "batch": args.batch,
                        "step_bytes": abytes,
-                       "l2": ("inputs larger than L2 (weights per step exceed 129 MB)" if args.workload == "step"
+                       "l2": ("inputs larger than L2 (weights per step exceed 129 MB)"
+                              if args.workload in ("step", "token")
                               else "inputs larger than L2 (blocks in + fp32 out exceed 129 MB)"
                               if args.workload in DEQUANT_TYPES
                               else "weights rotate over copies totalling at least 4x the 129 MB L2; "
@@ -668,11 +760,13 @@ def main():
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                          "traffic": traffic, "peak_source": peaks["source"],
                          "kernel": ("stream1_kernel (persistent plan launch)" if args.workload == "step"
+                                    else "whole token step (plan launches + attention + embedding decode)"
+                                    if args.workload == "token"
                                     else "dequant_kernel" if args.workload in DEQUANT_TYPES
                                     else "mma_gemv_kernel (tensor cores)"
                                     if args.batch >= mma_min_batch(levels[0][0].qtype)
                                     else "stream1_kernel (one GEMV per launch)")},
-            "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s",
+            "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s", "tok_s": round(world / e2e_s, 1),
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
