@@ -60,7 +60,9 @@ enum qdq_status {
     QDQ_ERR_CUDA = -5,     /* a CUDA runtime call or kernel launch failed */
     QDQ_ERR_TIMEOUT = -6,  /* a device-side bounded wait ran out (from qdq_get_device_status) */
     QDQ_ERR_DEVICE = -7,   /* current device is not sm_103 */
-    QDQ_ERR_LIMIT = -8     /* more GEMVs or levels than a plan supports */
+    QDQ_ERR_LIMIT = -8,    /* more GEMVs or levels than a plan supports */
+    QDQ_ERR_FORMAT = -9,   /* a malformed or truncated GGUF file */
+    QDQ_ERR_NOT_FOUND = -10 /* no such GGUF metadata key */
 };
 
 /* Bytes per block and weights per block of a type; -1 for an unknown type. */
@@ -272,6 +274,53 @@ int qdq_llama_buffers(const qdq_llama *model, float **logits, int64_t **argmax, 
                       uint16_t **k_cache, uint16_t **v_cache);
 int qdq_llama_launches(const qdq_llama *model);
 void qdq_llama_destroy(qdq_llama *model);
+
+/* ---------------------------------------------------------------------------
+ * qdq_quantize: fp32 values -> PETIT q8_0 or q4_0 blocks, the exporter's step
+ * ("PETIT", What makes it fast & small; How the pieces match: q8_0 = fp32 scale
+ * + 32 int8, q4_0 = fp16 scale + 16 nibble bytes read as (q - 8) * d, low
+ * nibbles = weights 0..15, values zero-padded to a multiple of 32).
+ * The scale rule is not on the pages; this library's reading, per block of 32:
+ *   q8_0: d = amax / 127, q = clamp(rint(x / d), -127, 127)   (q = 0 if d = 0)
+ *   q4_0: d = fp16(amax / 7), q = clamp(rint(x / d) + 8, 0, 15) (q = 8 if d = 0)
+ * with amax = max |x| over the block and every operation in binary32 (the
+ * division correctly rounded, rint halving to even), so the codes are those of
+ * any CPU that follows the same steps. A q4_0 block whose amax / 7 exceeds the
+ * fp16 range (amax > 458528) gets d = inf, which the format cannot represent:
+ * its weights decode to NaN. x: n fp32 (device); blocks: ceil(n/32)
+ * blocks (device). Both 16-byte aligned. Asynchronous on `stream`.
+ * ------------------------------------------------------------------------- */
+int qdq_quantize(int type, const float *x, int64_t n, void *blocks, qdq_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * GGUF container, read from memory (for instance a mapped file): header,
+ * metadata, tensor index ("S21 The Capstone: picoLM, in Python", section 1:
+ * a header, self-describing metadata, a tensor index of (name, shape, type,
+ * offset), padding to general.alignment, then one blob; each tensor is a byte
+ * range at a known offset). Host-only, no device work; every read is bounds
+ * checked (QDQ_ERR_FORMAT for a bad magic or version, a truncated file, an
+ * offset that is not a multiple of the alignment or runs past the end).
+ * qdq_gguf_parse fills up to max_tensors entries (QDQ_ERR_LIMIT if the file has
+ * more) with the tensors' names, dims (dims[0] innermost: the row length),
+ * GGUF type code, the library type that decodes it (QDQ_Q4_0 for type 2,
+ * QDQ_Q4_K for 12, QDQ_Q6_K for 14, else 0), absolute byte offset and size.
+ * qdq_gguf_find_kv locates a metadata value: its GGUF value type and the byte
+ * offset of the value (QDQ_ERR_NOT_FOUND if the key is absent).
+ * ------------------------------------------------------------------------- */
+typedef struct qdq_gguf_tensor {
+    char name[96];
+    int32_t n_dims;
+    int32_t ggml_type;
+    int32_t qdq_type;
+    int32_t reserved;
+    int64_t dims[4];
+    int64_t offset;
+    int64_t bytes;
+} qdq_gguf_tensor;
+int qdq_gguf_parse(const void *file, int64_t size, qdq_gguf_tensor *tensors, int max_tensors,
+                   int *n_tensors, int64_t *data_offset, uint32_t *alignment);
+int qdq_gguf_find_kv(const void *file, int64_t size, const char *key, uint32_t *value_type,
+                     int64_t *value_offset);
 
 /* ---------------------------------------------------------------------------
  * Device status: synchronises `stream`, returns the first device-side error

@@ -63,7 +63,8 @@ def quantize_q4_0(x: np.ndarray) -> np.ndarray:
     for b in range(xb.shape[0]):
         v = xb[b]
         amax = np.float32(np.max(np.abs(v)))
-        d16 = np.float16(np.float32(amax / np.float32(7.0)))
+        with np.errstate(over="ignore"):  # amax / 7 above 65504 has no finite fp16 scale: d = inf
+            d16 = np.float16(np.float32(amax / np.float32(7.0)))
         d = np.float32(d16)
         if d == 0:
             q = np.full(QK, 8, dtype=np.uint8)

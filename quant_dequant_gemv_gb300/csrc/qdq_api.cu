@@ -148,6 +148,8 @@ const char *qdq_status_string(int status) {
         case QDQ_ERR_TIMEOUT: return "a device-side bounded wait ran out";
         case QDQ_ERR_DEVICE: return "current device is not sm_103 (GB300)";
         case QDQ_ERR_LIMIT: return "too many GEMVs or levels for a plan, or batch too large for it";
+        case QDQ_ERR_FORMAT: return "malformed or truncated GGUF data";
+        case QDQ_ERR_NOT_FOUND: return "no such GGUF metadata key";
         default: return "unknown status";
     }
 }

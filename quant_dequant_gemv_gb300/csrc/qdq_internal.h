@@ -23,6 +23,7 @@ int check_descs(const qdq_gemv_desc *descs, int n, int batch, int device);
 int check_levels(const int *level, int n, int max_levels, int *nlevels);
 
 int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStream_t stream, int sm_count);
+int launch_quantize(int type, const float *x, int64_t n, void *blocks, cudaStream_t stream, int sm_count);
 
 // The streaming (CUDA-core) GEMV over a list of GEMVs grouped in dependency levels.
 struct StreamPlanHost;  // opaque: the packed kernel arguments

@@ -54,6 +54,12 @@ class LlamaLayer(ctypes.Structure):
                 ("attn_norm", _P), ("ffn_norm", _P)]
 
 
+class GgufTensor(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 96), ("n_dims", ctypes.c_int32), ("ggml_type", ctypes.c_int32),
+                ("qdq_type", ctypes.c_int32), ("reserved", ctypes.c_int32), ("dims", _I64 * 4),
+                ("offset", _I64), ("bytes", _I64)]
+
+
 def lib() -> ctypes.CDLL:
     """Load libqdq.so (built by __graft_entry__.build()). Raises if it is absent."""
     global _lib
@@ -92,6 +98,11 @@ def lib() -> ctypes.CDLL:
                                          ctypes.POINTER(_P), ctypes.POINTER(_P)]),
             "qdq_llama_launches": (_INT, [_P]),
             "qdq_llama_destroy": (None, [_P]),
+            "qdq_quantize": (_INT, [_INT, _P, _I64, _P, _P]),
+            "qdq_gguf_parse": (_INT, [_P, _I64, ctypes.POINTER(GgufTensor), _INT, ctypes.POINTER(_INT),
+                                      ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_uint32)]),
+            "qdq_gguf_find_kv": (_INT, [_P, _I64, ctypes.c_char_p, ctypes.POINTER(ctypes.c_uint32),
+                                        ctypes.POINTER(_I64)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -108,7 +119,8 @@ EXPORTS = ["qdq_block_bytes", "qdq_block_weights", "qdq_status_string", "qdq_dev
            "qdq_plan_run", "qdq_plan_run_io", "qdq_plan_reset", "qdq_plan_destroy",
            "qdq_plan_launches", "qdq_get_device_status", "qdq_selftest_wait_timeout",
            "qdq_gemv_levels_noalloc", "qdq_rope_attention", "qdq_llama_create", "qdq_llama_forward",
-           "qdq_llama_buffers", "qdq_llama_launches", "qdq_llama_destroy"]
+           "qdq_llama_buffers", "qdq_llama_launches", "qdq_llama_destroy", "qdq_quantize", "qdq_gguf_parse",
+           "qdq_gguf_find_kv"]
 
 
 def _ptr(t) -> int:
@@ -310,3 +322,34 @@ class Llama:
             self.close()
         except Exception:
             pass
+
+
+def quantize(qtype: int, x, n: int, blocks, stream=None) -> None:
+    """fp32 -> q8_0 / q4_0 blocks on the GPU (qdq_quantize)."""
+    _check(lib().qdq_quantize(qtype, _ptr(x), n, _ptr(blocks), _stream(stream)), "qdq_quantize")
+
+
+def gguf_parse(buf, max_tensors: int = 4096) -> tuple[list[dict], int, int]:
+    """Tensor index of GGUF bytes in host memory (a bytes object, numpy array or
+    mmap): ([{name, dims, ggml_type, qdq_type, offset, bytes}], data_offset, alignment)."""
+    import numpy as np
+    a = np.frombuffer(buf, dtype=np.uint8)
+    arr = (GgufTensor * max(max_tensors, 1))()
+    n, data, align = _INT(), _I64(), ctypes.c_uint32()
+    _check(lib().qdq_gguf_parse(a.ctypes.data, a.size, arr, max_tensors, ctypes.byref(n), ctypes.byref(data),
+                                ctypes.byref(align)), "qdq_gguf_parse")
+    out = []
+    for t in arr[:n.value]:
+        out.append({"name": t.name.decode(), "dims": list(t.dims[:t.n_dims]), "ggml_type": t.ggml_type,
+                    "qdq_type": t.qdq_type, "offset": t.offset, "bytes": t.bytes})
+    return out, data.value, align.value
+
+
+def gguf_find_kv(buf, key: str) -> tuple[int, int]:
+    """(GGUF value type, byte offset of the value) of a metadata key."""
+    import numpy as np
+    a = np.frombuffer(buf, dtype=np.uint8)
+    t, off = ctypes.c_uint32(), _I64()
+    _check(lib().qdq_gguf_find_kv(a.ctypes.data, a.size, key.encode(), ctypes.byref(t), ctypes.byref(off)),
+           "qdq_gguf_find_kv")
+    return t.value, off.value
