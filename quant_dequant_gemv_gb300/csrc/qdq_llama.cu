@@ -25,21 +25,29 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kMaxHeadDim = 256;
 
+// Pair frequencies base^(-2i / head_dim), computed on the host in double.
+struct RopeFreqs {
+    double f[kMaxHeadDim / 2];
+};
+
 // One CTA per query head h (KV head g = h / kv_mul).
-//  1. Angles of the pairs in double precision: pos * base^(-2i / head_dim) reaches
-//     thousands of radians, where a float angle would be off by 1e-4.
+//  1. Angles: pos * f_i reaches thousands of radians, where a float angle would
+//     be off by 1e-4. The product and its reduction by 2 pi are formed in double
+//     (four double operations: the frequencies come from the host, as double
+//     transcendentals are slow on this GPU), then sincosf of the reduced angle.
 //  2. q_h and k_g turn pair by pair; k and v are rounded to fp16 (the cache is
 //     fp16), and the first query head of the group stores them at position pos.
-//  3. Online softmax over t <= pos: warp w takes t = w, w + 8, ...; each keeps a
-//     running maximum m, sum l and weighted value sum, rescaled when m grows;
-//     the warps' states are merged at the end. No score array exists. The
-//     current position's key and value come from shared memory (their fp16
-//     values), so no CTA reads a cache entry another CTA is writing.
+//  3. Online softmax over t <= pos in chunks of 32 positions: warp w takes chunks
+//     w, w + 8, ...; each keeps a running maximum m, sum l and weighted value
+//     sum, rescaled when m grows; the warps' states are merged at the end. No
+//     score array exists. The current position's key and value come from shared
+//     memory (their fp16 values), so no CTA reads a cache entry another CTA is
+//     writing.
 __global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__restrict__ q, const float *__restrict__ k,
                                                                  const float *__restrict__ v, __half *k_cache,
                                                                  __half *v_cache, float *__restrict__ out,
                                                                  int n_heads, int n_kv_heads, int D, int pos,
-                                                                 float rope_base) {
+                                                                 const __grid_constant__ RopeFreqs fr) {
     __shared__ float qs[kMaxHeadDim], kc[kMaxHeadDim], vc[kMaxHeadDim];
     __shared__ float wm[kAttnWarps], wl[kAttnWarps];
     __shared__ float wacc[kAttnWarps][kMaxHeadDim];
@@ -49,8 +57,11 @@ __global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__
     const bool writer = (h % kv_mul) == 0;
 
     for (int i = tid; i < D / 2; i += kAttnThreads) {
-        const double th = (double)pos * pow((double)rope_base, -2.0 * (double)i / (double)D);
-        const float c = (float)cos(th), s = (float)sin(th);
+        const double th = (double)pos * fr.f[i];
+        const double kq = rint(th * 0.15915494309189535);  // turns: th / (2 pi)
+        const float r = (float)fma(-kq, 6.283185307179586, th);
+        float s, c;
+        sincosf(r, &s, &c);
         const float qa = q[h * D + 2 * i], qb = q[h * D + 2 * i + 1];
         qs[2 * i] = qa * c - qb * s;
         qs[2 * i + 1] = qa * s + qb * c;
@@ -72,29 +83,80 @@ __global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__
     __syncthreads();
 
     const float inv = 1.0f / sqrtf((float)D);
-    constexpr int kPer = kMaxHeadDim / 32;  // dims per lane: d = lane + 32 j
+    constexpr int kPer2 = kMaxHeadDim / 64;  // dim pairs per lane in the value sums
+    constexpr int kPer = 2 * kPer2;          // acc[2 j], acc[2 j + 1]: dims 2 (lane + 32 j), + 1
     float m = -INFINITY, l = 0.f, acc[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
-    for (int t = warp; t <= pos; t += kAttnWarps) {
-        const __half *kr = k_cache + (int64_t)t * kvd + g * D;
-        const __half *vr = v_cache + (int64_t)t * kvd + g * D;
-        float dot = 0.f;
+    const bool vec = (D & 7) == 0;  // key rows as 16-byte loads
+    // Warp w takes the 32-position chunks w, w + 8, ...: lane i scores position
+    // c0 + i over the whole head (its row's loads independent of the other
+    // lanes'), the chunk's maximum and weights come from warp reductions, then
+    // the lanes switch to dims and add the chunk's weighted values.
+    for (int c0 = 32 * warp; c0 <= pos; c0 += 32 * kAttnWarps) {
+        const int t = c0 + lane;
+        float s = -INFINITY;
+        if (t <= pos) {
+            float dot = 0.f;
+            if (t == pos) {
+                for (int d = 0; d < D; ++d) dot += qs[d] * kc[d];
+            } else if (vec) {
+                const uint4 *kr = reinterpret_cast<const uint4 *>(k_cache + (int64_t)t * kvd + g * D);
+                for (int e = 0; e < D / 8; ++e) {
+                    const uint4 u = kr[e];
+                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&u);
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int d = lane + 32 * j;
-            if (d < D) dot += qs[d] * (t == pos ? kc[d] : __half2float(kr[d]));
+                    for (int i = 0; i < 4; ++i) {
+                        const float2 f = __half22float2(h2[i]);
+                        dot += qs[8 * e + 2 * i] * f.x + qs[8 * e + 2 * i + 1] * f.y;
+                    }
+                }
+            } else {
+                const __half *kr = k_cache + (int64_t)t * kvd + g * D;
+                for (int d = 0; d < D; ++d) dot += qs[d] * __half2float(kr[d]);
+            }
+            s = dot * inv;
         }
+        float cm = s;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-        const float s = dot * inv;
-        const float mn = fmaxf(m, s);
-        const float scale = expf(m - mn), p = expf(s - mn);
-        l = l * scale + p;
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+        const float mn = fmaxf(m, cm);
+        const float scale = expf(m - mn);  // 0 for the first chunk (m = -inf)
+        const float p = t <= pos ? expf(s - mn) : 0.f;
+        float ps = p;
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int d = lane + 32 * j;
-            if (d < D) acc[j] = acc[j] * scale + p * (t == pos ? vc[d] : __half2float(vr[d]));
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, o);
+        l = l * scale + ps;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) acc[j] *= scale;
+        // weighted values: lane holds the dim pairs 2 lane + 64 j; positions before
+        // pos from the cache (independent loads), pos itself from shared memory
+        const int last = pos - c0 < 31 ? pos - c0 : 31;  // the chunk's last position, relative
+        const int nh = c0 + last == pos ? last : last + 1;  // ... of them in the cache
+        const __half2 *vrow = reinterpret_cast<const __half2 *>(v_cache + (int64_t)c0 * kvd + g * D);
+#pragma unroll 8
+        for (int u = 0; u < nh; ++u) {
+            const float pu = __shfl_sync(0xFFFFFFFFu, p, u);
+#pragma unroll
+            for (int j = 0; j < kPer2; ++j) {
+                const int d2 = lane + 32 * j;  // pair index
+                if (2 * d2 < D) {
+                    const float2 f = __half22float2(vrow[(int64_t)u * (kvd / 2) + d2]);
+                    acc[2 * j] += pu * f.x;
+                    acc[2 * j + 1] += pu * f.y;
+                }
+            }
+        }
+        if (nh <= last) {  // pos is in this chunk
+            const float pu = __shfl_sync(0xFFFFFFFFu, p, last);
+#pragma unroll
+            for (int j = 0; j < kPer2; ++j) {
+                const int d2 = lane + 32 * j;
+                if (2 * d2 < D) {
+                    acc[2 * j] += pu * vc[2 * d2];
+                    acc[2 * j + 1] += pu * vc[2 * d2 + 1];
+                }
+            }
         }
         m = mn;
     }
@@ -103,9 +165,12 @@ __global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__
         wl[warp] = l;
     }
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int d = lane + 32 * j;
-        if (d < D) wacc[warp][d] = acc[j];
+    for (int j = 0; j < kPer2; ++j) {
+        const int d2 = lane + 32 * j;
+        if (2 * d2 < D) {
+            wacc[warp][2 * d2] = acc[2 * j];
+            wacc[warp][2 * d2 + 1] = acc[2 * j + 1];
+        }
     }
     __syncthreads();
     float M = -INFINITY;
@@ -126,8 +191,10 @@ __global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__
 int launch_rope_attention(const float *q, const float *k, const float *v, uint16_t *k_cache, uint16_t *v_cache,
                           float *out, int n_heads, int n_kv_heads, int head_dim, int pos, float rope_base,
                           cudaStream_t stream) {
+    RopeFreqs fr;
+    for (int i = 0; i < head_dim / 2; ++i) fr.f[i] = std::pow((double)rope_base, -2.0 * i / (double)head_dim);
     rope_attn_kernel<<<n_heads, kAttnThreads, 0, stream>>>(q, k, v, (__half *)k_cache, (__half *)v_cache, out,
-                                                           n_heads, n_kv_heads, head_dim, pos, rope_base);
+                                                           n_heads, n_kv_heads, head_dim, pos, fr);
     if (cudaGetLastError() != cudaSuccess) return QDQ_ERR_CUDA;
     return QDQ_OK;
 }
