@@ -257,8 +257,10 @@ static int check_opts(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
     return rc;
 }
 
-int qdq_plan_create_ex(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n, int batch,
-                       qdq_plan **plan_out) {
+// Plan creation; with allow_attn, descriptors of type kPlanAttnType are attention
+// levels packed by the model (qdq_llama.cu) and skip the GEMV checks.
+static int plan_create(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n, int batch,
+                       bool allow_attn, qdq_plan **plan_out) {
     if (plan_out == nullptr || level == nullptr) return QDQ_ERR_PTR;
     *plan_out = nullptr;
     if (n < 1 || n > kMaxPlanDescs) return QDQ_ERR_LIMIT;
@@ -269,9 +271,25 @@ int qdq_plan_create_ex(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, co
     if (rc) return rc;
     const DeviceInfo &dev = current_device(&rc);
     if (rc) return rc;
-    if ((rc = check_descs(descs, n, batch, dev.device))) return rc;
+    // the GEMVs (every descriptor unless attention levels are allowed)
+    std::vector<qdq_gemv_desc> gd;
+    std::vector<qdq_gemv_opts> go;
+    std::vector<int> gl;
+    for (int i = 0; i < n; ++i) {
+        if (allow_attn && descs[i].type == kPlanAttnType) {
+            if (batch != 1) return QDQ_ERR_SHAPE;
+            continue;
+        }
+        gd.push_back(descs[i]);
+        if (opts) go.push_back(opts[i]);
+        gl.push_back(level[i]);
+    }
+    if ((rc = check_descs(gd.data(), (int)gd.size(), batch, dev.device))) return rc;
     bool has_argmax = false;
-    if ((rc = check_opts(descs, opts, level, n, batch, dev.device, &has_argmax))) return rc;
+    if (!gd.empty() &&
+        (rc = check_opts(gd.data(), opts ? go.data() : nullptr, gl.data(), (int)gd.size(), batch, dev.device,
+                         &has_argmax)))
+        return rc;
     qdq_plan *p = new (std::nothrow) qdq_plan();
     if (!p) return QDQ_ERR_CUDA;
     p->device = dev.device;
@@ -296,6 +314,11 @@ int qdq_plan_create_ex(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, co
         return fail(rc);
     *plan_out = p;
     return QDQ_OK;
+}
+
+int qdq_plan_create_ex(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n, int batch,
+                       qdq_plan **plan_out) {
+    return plan_create(descs, opts, level, n, batch, false, plan_out);
 }
 
 int qdq_plan_run(qdq_plan *plan, qdq_stream_t stream) {
@@ -389,3 +412,15 @@ int qdq_selftest_wait_timeout(int64_t timeout_ns, qdq_stream_t stream) {
 }
 
 }  // extern "C"
+
+namespace qdq {
+int plan_create_with_attention(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n,
+                               qdq_plan **plan_out) {
+    return plan_create(descs, opts, level, n, 1, true, plan_out);
+}
+int plan_set_pos(qdq_plan *plan, int pos) {
+    if (plan == nullptr) return QDQ_ERR_PTR;
+    stream_plan_set_pos(plan->host, pos);
+    return QDQ_OK;
+}
+}  // namespace qdq

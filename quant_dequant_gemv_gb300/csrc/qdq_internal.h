@@ -33,6 +33,20 @@ int stream_plan_build(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
                       int batch, unsigned *counters, unsigned long long *amax_slot, int sm_count,
                       StreamPlanHost **out);
 int stream_plan_launch(const StreamPlanHost *p, cudaStream_t stream);
+// The position attention levels of the plan run at (the next launches).
+void stream_plan_set_pos(StreamPlanHost *p, int pos);
+
+// A plan level that is not a GEMV: the attention block of one position, one query
+// head per CTA (qdq_stream1.cu, attend). Packed as a descriptor of type
+// kTypeAttn (64) with W = the key cache, x = q, y = the output, rows = query
+// heads, cols = head_dim, and its options holding x2 = k, norm_w = v, argmax =
+// the value cache, reserved = KV heads, eps = the RoPE base. Alone in its level.
+constexpr int kPlanAttnType = 64;
+// qdq_plan_create_ex for plans that also hold attention levels: the GEMVs are
+// checked as there; the attention descriptors are the caller's (the model's).
+int plan_create_with_attention(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, const int *level, int n,
+                               qdq_plan **plan_out);
+int plan_set_pos(qdq_plan *plan, int pos);
 void stream_plan_free(StreamPlanHost *p);
 int stream_plan_nlevels(const StreamPlanHost *p);
 int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, int n, int batch,
@@ -41,7 +55,7 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
 int take_status_stream();
 // The streaming kernel (qdq_stream1.cu) at batch width bt (1, 2, 4 or 8): runs the
 // argument block packed by the plan functions above.
-int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, cudaStream_t stream);
+int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, bool attn, cudaStream_t stream);
 int take_status_stream1();
 int launch_wait_selftest(int64_t limit_ns, cudaStream_t stream);
 

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kAttnThreads) rope_attn_kernel(const float *__
         const double kq = rint(th * 0.15915494309189535);  // turns: th / (2 pi)
         const float r = (float)fma(-kq, 6.283185307179586, th);
         float s, c;
-        sincosf(r, &s, &c);
+        __sincosf(r, &s, &c);  // |r| <= pi: the fast form is accurate to ~4e-7
         const float qa = q[h * D + 2 * i], qb = q[h * D + 2 * i + 1];
         qs[2 * i] = qa * c - qb * s;
         qs[2 * i + 1] = qa * s + qb * c;
@@ -219,8 +219,7 @@ struct qdq_llama {
           *logits = nullptr;
     int64_t *argmax = nullptr;
     uint16_t *kcache = nullptr, *vcache = nullptr;
-    qdq_plan *first = nullptr;             // q/k/v of layer 0
-    std::vector<qdq_plan *> layer_plans;  // layer l: o, gate/up, down, then q/k/v of l+1 or the head
+    qdq_plan *plan = nullptr;  // every layer and the head, attention levels included
 };
 
 namespace {
@@ -332,53 +331,50 @@ int qdq_llama_create(const qdq_llama_config *cfg, const void *token_embd, int em
     std::vector<qdq_gemv_desc> D;
     std::vector<qdq_gemv_opts> O;
     std::vector<int> Lv;
-    // q, k, v of layer l read rmsnorm(h, attn_norm[l]) (one staged x for the three)
-    auto add_qkv = [&](int l, int level) {
+    int level = 0;
+    const int D_h = cfg->dim / cfg->n_heads;
+    for (int l = 0; l < cfg->n_layers; ++l) {
         const qdq_llama_layer &w = layers[l];
-        const float *nw = w.attn_norm;
+        // q, k, v read rmsnorm(h, attn_norm) (one staged x for the three)
         D.push_back(desc(w.type[0], w.w[0], dim, dim, m->h, m->q));
         D.push_back(desc(w.type[1], w.w[1], kv, dim, m->h, m->k));
         D.push_back(desc(w.type[2], w.w[2], kv, dim, m->h, m->v));
         for (int i = 0; i < 3; ++i) {
-            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, nw, eps, nullptr));
+            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, w.attn_norm, eps, nullptr));
             Lv.push_back(level);
         }
-    };
-    auto make = [&](qdq_plan **p) {
-        const int r = qdq_plan_create_ex(D.data(), O.data(), Lv.data(), (int)D.size(), 1, p);
-        D.clear();
-        O.clear();
-        Lv.clear();
-        return r;
-    };
-    add_qkv(0, 0);
-    rc = make(&m->first);
-    for (int l = 0; l < cfg->n_layers && !rc; ++l) {
-        const qdq_llama_layer &w = layers[l];
+        ++level;
+        // attention of this layer: its own level (see kPlanAttnType for the packing)
+        qdq_gemv_desc a = desc(kPlanAttnType, m->kcache + (int64_t)l * cfg->max_seq * kv, cfg->n_heads, D_h, m->q,
+                               m->att);
+        qdq_gemv_opts ao = opt(QDQ_X_PLAIN, QDQ_Y_STORE, m->k, m->v, cfg->rope_base,
+                               (int64_t *)(m->vcache + (int64_t)l * cfg->max_seq * kv));
+        ao.reserved = cfg->n_kv_heads;
+        D.push_back(a);
+        O.push_back(ao);
+        Lv.push_back(level++);
         // h += Wo att; gate, up from rmsnorm(h, ffn_norm); h += Wdown (silu(gate) * up)
         D.push_back(desc(w.type[3], w.w[3], dim, dim, m->att, m->h));
         O.push_back(opt(QDQ_X_PLAIN, QDQ_Y_ADD, nullptr, nullptr, 0.f, nullptr));
-        Lv.push_back(0);
+        Lv.push_back(level++);
         D.push_back(desc(w.type[4], w.w[4], hid, dim, m->h, m->gate));
         D.push_back(desc(w.type[5], w.w[5], hid, dim, m->h, m->up));
         for (int i = 0; i < 2; ++i) {
             O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, w.ffn_norm, eps, nullptr));
-            Lv.push_back(1);
+            Lv.push_back(level);
         }
+        ++level;
         D.push_back(desc(w.type[6], w.w[6], dim, hid, m->gate, m->h));
         O.push_back(opt(QDQ_X_SWIGLU, QDQ_Y_ADD, m->up, nullptr, 0.f, nullptr));
-        Lv.push_back(2);
-        if (l + 1 < cfg->n_layers) {
-            add_qkv(l + 1, 3);
-        } else {  // logits = Wout rmsnorm(h, output_norm), with their argmax
-            D.push_back(desc(output_type, output, cfg->vocab, dim, m->h, m->logits));
-            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, output_norm, eps, m->argmax));
-            Lv.push_back(3);
-        }
-        qdq_plan *p = nullptr;
-        rc = make(&p);
-        if (!rc) m->layer_plans.push_back(p);
+        Lv.push_back(level++);
     }
+    // logits = Wout rmsnorm(h, output_norm), with their argmax
+    D.push_back(desc(output_type, output, cfg->vocab, dim, m->h, m->logits));
+    O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, output_norm, eps, m->argmax));
+    Lv.push_back(level);
+    rc = (int)D.size() > kMaxPlanDescs || level + 1 > kMaxPlanLevels
+             ? QDQ_ERR_LIMIT
+             : plan_create_with_attention(D.data(), O.data(), Lv.data(), (int)D.size(), &m->plan);
     if (rc) {
         qdq_llama_destroy(m);
         return rc;
@@ -392,19 +388,12 @@ int qdq_llama_forward(qdq_llama *m, int token, int pos, qdq_stream_t stream) {
     if (token < 0 || token >= m->cfg.vocab || pos < 0 || pos >= m->cfg.max_seq) return QDQ_ERR_SHAPE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != m->device) return QDQ_ERR_DEVICE;
-    const cudaStream_t s = (cudaStream_t)stream;
     const qdq_llama_config &c = m->cfg;
-    const int D = c.dim / c.n_heads;
-    const int64_t kvl = (int64_t)c.max_seq * c.n_kv_heads * D;  // cache entries of one layer
-    // x = the token's embedding row, decoded
+    // x = the token's embedding row, decoded; then every layer and the head in one launch
     int rc = qdq_dequant_async(m->embd_type, (const char *)m->embd + (int64_t)token * m->embd_row_bytes, c.dim, m->h,
                                stream);
-    if (!rc) rc = qdq_plan_run(m->first, stream);
-    for (int l = 0; l < c.n_layers && !rc; ++l) {
-        rc = launch_rope_attention(m->q, m->k, m->v, m->kcache + l * kvl, m->vcache + l * kvl, m->att, c.n_heads,
-                                   c.n_kv_heads, D, pos, c.rope_base, s);
-        if (!rc) rc = qdq_plan_run(m->layer_plans[l], stream);
-    }
+    if (!rc) rc = plan_set_pos(m->plan, pos);
+    if (!rc) rc = qdq_plan_run(m->plan, stream);
     return rc;
 }
 
@@ -419,12 +408,11 @@ int qdq_llama_buffers(const qdq_llama *m, float **logits, int64_t **argmax, floa
     return QDQ_OK;
 }
 
-int qdq_llama_launches(const qdq_llama *m) { return m ? 2 + 2 * m->cfg.n_layers : 0; }
+int qdq_llama_launches(const qdq_llama *m) { return m ? 2 : 0; }
 
 void qdq_llama_destroy(qdq_llama *m) {
     if (m == nullptr) return;
-    if (m->first) qdq_plan_destroy(m->first);
-    for (qdq_plan *p : m->layer_plans) qdq_plan_destroy(p);
+    if (m->plan) qdq_plan_destroy(m->plan);
     if (m->mem) cudaFree(m->mem);
     delete m;
 }

@@ -7,6 +7,7 @@
 // projections of a decode step, each reading the previous one's output, which
 // is what the dependency levels encode); "PETIT" (gemv_q8 / gemv_q4, weights
 // stored out x in).
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -33,6 +34,7 @@ struct StreamPlanHost {
     size_t args_bytes;
     void *args;  // StreamArgs<...>
     bool big;
+    bool attn;  // the plan has attention levels
 };
 
 #ifdef QDQ_TRACE
@@ -59,6 +61,22 @@ static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, con
     A->level_start[L + 1] = n;
     for (int i = 0; i < n; ++i) {
         DevDesc &d = A->d[i];
+        DescEx &e = A->ex[i];
+        if (descs[i].type == kTypeAttn) {  // packed as kPlanAttnType describes
+            d.type = kTypeAttn;
+            d.x = descs[i].x;
+            d.y = descs[i].y;
+            d.rows = descs[i].rows;
+            d.cols = (int32_t)descs[i].cols;
+            d.nkv = opts[i].reserved;
+            e.kc = (uint16_t *)descs[i].W;
+            e.vc = (uint16_t *)opts[i].argmax;
+            e.x2 = opts[i].x2;
+            e.nw = opts[i].norm_w;
+            for (int p = 0; p < d.cols / 2 && p < kMaxRopePairs; ++p)
+                A->rope_f[p] = std::pow((double)opts[i].eps, -2.0 * p / (double)d.cols);
+            continue;
+        }
         d.W = (const uint8_t *)descs[i].W;
         d.x = descs[i].x;
         d.y = descs[i].y;
@@ -67,13 +85,11 @@ static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, con
         d.type = descs[i].type;
         d.rb = (int32_t)((descs[i].cols / blk_weights(d.type)) * blk_bytes(d.type));
         if (opts) {
-            d.xop = opts[i].x_op;
-            d.yop = opts[i].y_op;
-            d.x2 = opts[i].x2;
-            d.nw = opts[i].norm_w;
-            d.eps = opts[i].eps;
+            d.ops = (opts[i].x_op & 15) | ((opts[i].y_op & 15) << 4) | (opts[i].argmax ? 256 : 0);
+            e.x2 = opts[i].x2;
+            e.nw = opts[i].norm_w;
+            e.eps = opts[i].eps;
             if (opts[i].argmax) {
-                d.amax = 1;
                 A->amax_slot = amax_slot;
                 A->amax_y = descs[i].y;
                 A->amax_out = (long long *)opts[i].argmax;
@@ -85,7 +101,7 @@ static void fill_args(StreamArgs<MAXD, MAXL> *A, const qdq_gemv_desc *descs, con
         for (int i = A->level_start[lv]; i < A->level_start[lv + 1]; ++i) {
             int kinds = 0;
             for (int k = A->level_start[lv]; k < A->level_start[lv + 1]; ++k)
-                if (A->d[k].x == A->d[i].x) kinds |= 1 << x_kind(A->d[k].type);
+                if (A->d[k].x == A->d[i].x && A->d[k].type != kTypeAttn) kinds |= 1 << x_kind(A->d[k].type);
             A->d[i].kinds = kinds;
         }
     }
@@ -102,6 +118,8 @@ int stream_plan_build(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
     const int nlev = level ? level[n - 1] + 1 : 1;
     p->big = n > kMaxGroupDescs || nlev > 1;
     p->cooperative = nlev > 1;
+    p->attn = false;
+    for (int i = 0; i < n; ++i) p->attn = p->attn || descs[i].type == kTypeAttn;
     if (p->big) {
         using A = StreamArgs<kMaxPlanDescs, kMaxPlanLevels>;
         A *args = (A *)malloc(sizeof(A));
@@ -121,8 +139,15 @@ int stream_plan_build(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
     return QDQ_OK;
 }
 
+void stream_plan_set_pos(StreamPlanHost *p, int pos) {
+    if (p->big)
+        ((StreamArgs<kMaxPlanDescs, kMaxPlanLevels> *)p->args)->attn_pos = pos;
+    else
+        ((StreamArgs<kMaxGroupDescs, 1> *)p->args)->attn_pos = pos;
+}
+
 int stream_plan_launch(const StreamPlanHost *p, cudaStream_t stream) {
-    return stream1_launch(p->args, p->big, p->cooperative, p->grid, p->bt, stream);
+    return stream1_launch(p->args, p->big, p->cooperative, p->grid, p->bt, p->attn, stream);
 }
 
 // Multi-level launch with caller-provided level counters and no heap use: the
@@ -136,6 +161,7 @@ int stream_launch_levels_inplace(const qdq_gemv_desc *descs, const int *level, i
     p.grid = sm_count;
     p.big = true;
     p.cooperative = true;
+    p.attn = false;
     p.args = &args;
     p.args_bytes = sizeof(A);
     fill_args(&args, descs, nullptr, level, n, batch, counters, nullptr);

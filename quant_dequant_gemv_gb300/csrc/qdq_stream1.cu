@@ -37,6 +37,8 @@
 #include <cstdio>
 #include <type_traits>
 
+#include <cuda_fp16.h>
+
 #include "qdq_stream_common.cuh"
 
 namespace qdq {
@@ -147,6 +149,7 @@ struct Tile {
     bool first;       // first chunk of this row group in the window
     bool last;        // last chunk of this row group in the window
     bool first_win;   // the window starts at column 0 (y is stored, not accumulated)
+    bool attn;        // attention heads row0 .. row0 + nrows - 1 (no weights, no ring slot)
     int skinds;       // x copy kinds staged for this tile's epoch
 };
 
@@ -213,7 +216,7 @@ QDQ_DEV uint32_t ring_place(uint32_t &next, uint32_t bytes) {
 
 // on_begin(L) / on_end(L) around each level; on_tile(tile, epoch, desc) for every
 // tile. An epoch is one staged x window: (level, x, columns, window).
-template <int BT, class A, class FBegin, class FTile, class FEnd>
+template <int BT, bool ATTN, class A, class FBegin, class FTile, class FEnd>
 QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&on_tile, FEnd &&on_end) {
     int epoch = -1;
     for (int L = 0; L < a.nlevels; ++L) {
@@ -224,6 +227,15 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
             const int64_t ra = ranges[2 * g], rb = ranges[2 * g + 1];
             if (ra >= rb) continue;
             const DevDesc d = a.d[g];
+            if (ATTN && d.type == kTypeAttn) {
+                Tile t{};
+                t.g = g;
+                t.row0 = ra;
+                t.nrows = (int)(rb - ra);
+                t.attn = true;
+                on_tile(t, epoch, d);
+                continue;
+            }
             const int nch = (d.cols + kChunk - 1) / kChunk;
             const int n = (int)(rb - ra);  // rows of one GEMV on one CTA
             const int sk = staged_kinds<BT>(d);
@@ -237,7 +249,7 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
                     ekinds = sk;
                 }
                 for (int r = 0; r < n; r += wr) {
-                    Tile t;
+                    Tile t{};
                     t.g = g;
                     t.nrows = n - r < wr ? n - r : wr;
                     t.row0 = ra + r;
@@ -269,7 +281,7 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
                 for (int tg = 0; tg < ntg; ++tg) {
                     const int nr = nbase + (tg < nextra ? 1 : 0);
                     for (int j = w0; j < w1; ++j) {
-                        Tile t;
+                        Tile t{};
                         t.g = g;
                         t.nrows = nr;
                         t.row0 = r;
@@ -298,8 +310,17 @@ QDQ_DEV void walk(const A &a, const int64_t *ranges, FBegin &&on_begin, FTile &&
 // among its CTAs, so a CTA normally works on a single GEMV per level: one x
 // format and as few tiles as possible. A GEMV too small to earn a CTA of its own
 // goes whole to the CTA at its position.
-template <class A>
+template <bool ATTN, class A>
 QDQ_DEV void cta_rows_by_gemv(const A &a, int L, int g, int cta, int P, int64_t *ra, int64_t *rb) {
+    if (ATTN && a.d[g].type == kTypeAttn) {  // an attention level (alone in its level): heads over the CTAs
+        const int64_t heads = a.d[g].rows, n = heads < P ? heads : P;
+        *ra = *rb = 0;
+        if (cta < n) {
+            *ra = cta * heads / n;
+            *rb = (cta + 1) * heads / n;
+        }
+        return;
+    }
     int64_t total = 0, before = 0;
     for (int i = a.level_start[L]; i < a.level_start[L + 1]; ++i) {
         const int64_t bytes = a.d[i].rows * (int64_t)a.d[i].rb;
@@ -376,7 +397,8 @@ QDQ_DEV int xunit(int u) { return (u & ~15) | ((u & 15) ^ ((u >> 3) & 6)); }
 // window), then every thread adds the warps' sums in warp order, so every
 // thread holds the same inv.
 template <int BT>
-QDQ_DEV void rms_scale(const DevDesc &d, int batch, int cw, int ncw, int lane, float *red, float (&inv)[BT]) {
+QDQ_DEV void rms_scale(const DevDesc &d, const DescEx &ex, int batch, int cw, int ncw, int lane, float *red,
+                       float (&inv)[BT]) {
     float ss[BT];
 #pragma unroll
     for (int b = 0; b < BT; ++b) ss[b] = 0.f;
@@ -399,7 +421,7 @@ QDQ_DEV void rms_scale(const DevDesc &d, int batch, int cw, int ncw, int lane, f
     for (int b = 0; b < BT; ++b) {
         float t = 0.f;
         for (int w = 0; w < ncw; ++w) t += red[w * 8 + b];
-        inv[b] = 1.0f / sqrtf(t / (float)d.cols + d.eps);
+        inv[b] = 1.0f / sqrtf(t / (float)d.cols + ex.eps);
     }
 }
 
@@ -408,22 +430,23 @@ QDQ_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
 // The value the dot product reads at x[b][col..col+3] (QDQ_X_*): as stored,
 // rmsnorm-scaled, or silu(gate) * up.
 template <int BT>
-QDQ_DEV float4 x_in(const DevDesc &d, int b, int col, int off, const float (&inv)[BT], float4 v) {
-    if (d.xop == QDQ_X_RMSNORM) {
-        const float4 w = __ldg((const float4 *)(d.nw + col + off));
+QDQ_DEV float4 x_in(const DevDesc &d, const DescEx &ex, int b, int col, int off, const float (&inv)[BT], float4 v) {
+    const int xop = desc_xop(d);
+    if (xop == QDQ_X_RMSNORM) {
+        const float4 w = __ldg((const float4 *)(ex.nw + col + off));
         const float s = inv[b];
         return make_float4(v.x * s * w.x, v.y * s * w.y, v.z * s * w.z, v.w * s * w.w);
     }
-    if (d.xop == QDQ_X_SWIGLU) {
-        const float4 u = __ldcg((const float4 *)(d.x2 + (int64_t)b * d.cols + col + off));
+    if (xop == QDQ_X_SWIGLU) {
+        const float4 u = __ldcg((const float4 *)(ex.x2 + (int64_t)b * d.cols + col + off));
         return make_float4(silu(v.x) * u.x, silu(v.y) * u.y, silu(v.z) * u.z, silu(v.w) * u.w);
     }
     return v;
 }
 
 template <int BT>
-QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, int cw, int ncw, int lane,
-                      const float (&inv)[BT], float *xbuf) {
+QDQ_DEV void stage_xb(const DevDesc &d, const DescEx &ex, int kinds, int batch, int w0, int w1, int cw, int ncw,
+                      int lane, const float (&inv)[BT], float *xbuf) {
     const int nk = nkinds(kinds), stride = xfloats_per_chunk<BT>(kinds);
     const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
     for (int i = cw; i < (w1 - w0) * kSlicesPerChunk; i += ncw) {
@@ -434,9 +457,10 @@ QDQ_DEV void stage_xb(const DevDesc &d, int kinds, int batch, int w0, int w1, in
         for (int b = 0; b < BT; ++b) {
             const bool ok = b < batch && col < d.cols;
             const float *xr = d.x + (int64_t)b * d.cols + col;
-            const float4 a = ok ? x_in<BT>(d, b, col, 0, inv, __ldcg((const float4 *)xr)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 a =
+                ok ? x_in<BT>(d, ex, b, col, 0, inv, __ldcg((const float4 *)xr)) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float4 c =
-                ok ? x_in<BT>(d, b, col, 4, inv, __ldcg((const float4 *)(xr + 4))) : make_float4(0.f, 0.f, 0.f, 0.f);
+                ok ? x_in<BT>(d, ex, b, col, 4, inv, __ldcg((const float4 *)(xr + 4))) : make_float4(0.f, 0.f, 0.f, 0.f);
             int slot = 0;
             if (kinds & 1) {
                 float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
@@ -848,9 +872,165 @@ QDQ_DEV void tile_units1(const Tile &tl, const DevDesc &d, const uint8_t *stage_
 }
 
 // ---------------------------------------------------------------------------
+// An attention level ("S21 The Capstone: picoLM, in Python", section 4: rope on q
+// and k, the fp16 cache written at pos, per-head attention with an online
+// softmax and GQA; section 3: interleaved RoPE pairs). Query heads [row0, row0 +
+// nrows) of this CTA, by all consumer warps, the x buffer as scratch:
+//  * the pair angles pos * f_i formed and reduced by 2 pi in double (four double
+//    operations), sincosf of the reduced angle; q_h and k_g turned, k and v
+//    rounded to fp16; the group's first head stores them at row pos;
+//  * warp w scores the 32-position chunks w, w + NCW, ... (lane i: position
+//    c0 + i over the whole head) and adds the chunk's weighted values (lanes over
+//    dim pairs), keeping a running maximum, sum and value sum; the current
+//    position's key and value come from shared memory;
+//  * the warps' states merged in warp order into out[h].
+// q, k, v were written by the previous level on other SMs: read through L2.
+// ---------------------------------------------------------------------------
+constexpr int kAttnMaxD = 256;
+
+template <int NCW, class A>
+QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &tl, int ctid, int cw, int lane,
+                    float *scratch) {
+    const int D = d.cols, kvd = d.nkv * D, kv_mul = (int)d.rows / d.nkv, pos = a.attn_pos;
+    float *qs = scratch, *kcur = qs + kAttnMaxD, *vcur = kcur + kAttnMaxD;
+    float *wm = vcur + kAttnMaxD, *wl = wm + 32, *wacc = wl + 32;  // wacc[NCW][kAttnMaxD]
+    const __half *kc = reinterpret_cast<const __half *>(ex.kc), *vc = reinterpret_cast<const __half *>(ex.vc);
+    const float inv = 1.0f / sqrtf((float)D);
+    const bool vec = (D & 7) == 0;
+    constexpr int kPer2 = kAttnMaxD / 64;
+    for (int h = (int)tl.row0; h < (int)tl.row0 + tl.nrows; ++h) {
+        const int g = h / kv_mul;
+        const bool writer = h % kv_mul == 0;
+        for (int i = ctid; i < D / 2; i += NCW * 32) {
+            const double th = (double)pos * a.rope_f[i];
+            const double turns = rint(th * 0.15915494309189535);
+            float sn, cs;
+            __sincosf((float)fma(-turns, 6.283185307179586, th), &sn, &cs);  // |angle| <= pi: the fast form is accurate to ~4e-7
+            const float qa = __ldcg(d.x + h * D + 2 * i), qb = __ldcg(d.x + h * D + 2 * i + 1);
+            qs[2 * i] = qa * cs - qb * sn;
+            qs[2 * i + 1] = qa * sn + qb * cs;
+            const float ka = __ldcg(ex.x2 + g * D + 2 * i), kb = __ldcg(ex.x2 + g * D + 2 * i + 1);
+            const __half k0 = __float2half_rn(ka * cs - kb * sn), k1 = __float2half_rn(ka * sn + kb * cs);
+            const __half v0 = __float2half_rn(__ldcg(ex.nw + g * D + 2 * i));
+            const __half v1 = __float2half_rn(__ldcg(ex.nw + g * D + 2 * i + 1));
+            kcur[2 * i] = __half2float(k0);
+            kcur[2 * i + 1] = __half2float(k1);
+            vcur[2 * i] = __half2float(v0);
+            vcur[2 * i + 1] = __half2float(v1);
+            if (writer) {
+                const int64_t o = (int64_t)pos * kvd + g * D + 2 * i;
+                reinterpret_cast<__half *>(ex.kc)[o] = k0;
+                reinterpret_cast<__half *>(ex.kc)[o + 1] = k1;
+                reinterpret_cast<__half *>(ex.vc)[o] = v0;
+                reinterpret_cast<__half *>(ex.vc)[o + 1] = v1;
+            }
+        }
+        named_bar_sync(kFlushBar, NCW * 32);
+        float m = -INFINITY, l = 0.f, acc[2 * kPer2];
+#pragma unroll
+        for (int j = 0; j < 2 * kPer2; ++j) acc[j] = 0.f;
+        for (int c0 = 32 * cw; c0 <= pos; c0 += 32 * NCW) {
+            const int t = c0 + lane;
+            float s = -INFINITY;
+            if (t <= pos) {
+                float dot = 0.f;
+                if (t == pos) {
+                    for (int e = 0; e < D; ++e) dot += qs[e] * kcur[e];
+                } else if (vec) {
+                    const uint4 *kr = reinterpret_cast<const uint4 *>(kc + (int64_t)t * kvd + g * D);
+                    for (int e = 0; e < D / 8; ++e) {
+                        const uint4 u = __ldcg(kr + e);
+                        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float lo = __half2float(__ushort_as_half((unsigned short)(w4[i] & 0xFFFFu)));
+                            const float hi = __half2float(__ushort_as_half((unsigned short)(w4[i] >> 16)));
+                            dot += qs[8 * e + 2 * i] * lo + qs[8 * e + 2 * i + 1] * hi;
+                        }
+                    }
+                } else {
+                    const __half *kr = kc + (int64_t)t * kvd + g * D;
+                    for (int e = 0; e < D; ++e) dot += qs[e] * __half2float(kr[e]);
+                }
+                s = dot * inv;
+            }
+            float cm = s;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+            const float mn = fmaxf(m, cm);
+            const float scale = expf(m - mn);
+            const float p = t <= pos ? expf(s - mn) : 0.f;
+            float ps = p;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, o);
+            l = l * scale + ps;
+#pragma unroll
+            for (int j = 0; j < 2 * kPer2; ++j) acc[j] *= scale;
+            const int last = pos - c0 < 31 ? pos - c0 : 31;
+            const int nh = c0 + last == pos ? last : last + 1;
+            const __half2 *vrow = reinterpret_cast<const __half2 *>(vc + (int64_t)c0 * kvd + g * D);
+#pragma unroll 8
+            for (int u = 0; u < nh; ++u) {
+                const float pu = __shfl_sync(0xFFFFFFFFu, p, u);
+#pragma unroll
+                for (int j = 0; j < kPer2; ++j) {
+                    const int d2 = lane + 32 * j;
+                    if (2 * d2 < D) {
+                        const float2 f = __half22float2(__ldcg(vrow + (int64_t)u * (kvd / 2) + d2));
+                        acc[2 * j] += pu * f.x;
+                        acc[2 * j + 1] += pu * f.y;
+                    }
+                }
+            }
+            if (nh <= last) {
+                const float pu = __shfl_sync(0xFFFFFFFFu, p, last);
+#pragma unroll
+                for (int j = 0; j < kPer2; ++j) {
+                    const int d2 = lane + 32 * j;
+                    if (2 * d2 < D) {
+                        acc[2 * j] += pu * vcur[2 * d2];
+                        acc[2 * j + 1] += pu * vcur[2 * d2 + 1];
+                    }
+                }
+            }
+            m = mn;
+        }
+        if (lane == 0) {
+            wm[cw] = m;
+            wl[cw] = l;
+        }
+#pragma unroll
+        for (int j = 0; j < kPer2; ++j) {
+            const int d2 = lane + 32 * j;
+            if (2 * d2 < D) {
+                wacc[cw * kAttnMaxD + 2 * d2] = acc[2 * j];
+                wacc[cw * kAttnMaxD + 2 * d2 + 1] = acc[2 * j + 1];
+            }
+        }
+        named_bar_sync(kFlushBar, NCW * 32);
+        float M = -INFINITY, L = 0.f;
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, wm[w]);
+        for (int w = 0; w < NCW; ++w)
+            if (wl[w] > 0.f) L += wl[w] * expf(wm[w] - M);
+        for (int e = ctid; e < D; e += NCW * 32) {
+            float o = 0.f;
+            for (int w = 0; w < NCW; ++w)
+                if (wl[w] > 0.f) o += wacc[w * kAttnMaxD + e] * expf(wm[w] - M);
+            d.y[h * D + e] = o / L;
+        }
+        // the scratch is reused by the next head, and these stores precede the
+        // level's release
+        named_bar_sync(kFlushBar, NCW * 32);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-template <int BT, int MAXD, int MAXL>
+// ATTN: the plan has attention levels. Only that instantiation holds the attention
+// code: compiled into the tile callback of the others, it slowed their GEMV levels
+// by a few per cent (and by more as an out-of-line call).
+template <int BT, int MAXD, int MAXL, bool ATTN>
 __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __grid_constant__ StreamArgs<MAXD, MAXL> a) {
     using SM = Smem<BT, MAXD>;
     constexpr int kBufRows = Cfg<BT>::kBufRows;
@@ -880,7 +1060,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
     }
     for (int L = 0; L < a.nlevels; ++L)
         for (int g = a.level_start[L] + (int)threadIdx.x; g < a.level_start[L + 1]; g += kThreads)
-            cta_rows_by_gemv(a, L, g, cta, P, &ranges[2 * g], &ranges[2 * g + 1]);
+            cta_rows_by_gemv<ATTN>(a, L, g, cta, P, &ranges[2 * g], &ranges[2 * g + 1]);
     __syncthreads();
 
     if (warp == 0) {
@@ -893,13 +1073,14 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
         uint32_t next = 0;
         uint32_t *toff = (uint32_t *)(smem + SM::kRing), *tlen = toff + kSlots;
         int plevel = 0, ptile = 0;  // trace builds: level and tile within it
-        walk<BT>(
+        walk<BT, ATTN>(
             a, ranges,
             [&](int L) {
                 plevel = L;
                 ptile = 0;
             },
             [&](const Tile &tl, int, const DevDesc &d) {
+                if (tl.attn) return;  // no weights to stream
                 if (ptile == 0) S1_TR(plevel, 29);
                 const uint32_t bytes = tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols);
                 const uint32_t o = ring_place<BT>(next, bytes);
@@ -988,7 +1169,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
         buf_rows = 0;
     };
 
-    walk<BT>(
+    walk<BT, ATTN>(
         a, ranges,
         [&](int L) {
             cur_level = L;
@@ -1009,6 +1190,13 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 dep_pending = false;
                 cur_e = -1;  // x is read again after the dependency
             }
+            if constexpr (ATTN) {
+                if (tl.attn) {
+                    static_assert(3 * kAttnMaxD + 64 + kCW * kAttnMaxD <= Cfg<BT>::kXFloats, "attention scratch");
+                    attend<kCW>(a, d, a.ex[tl.g], tl, ctid, cw, lane, xbuf);
+                    return;
+                }
+            }
             if (e != cur_e) {
                 cur_e = e;
                 // the buffer is shared: a later x of the same level waits for every
@@ -1017,8 +1205,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 float inv[BT];
 #pragma unroll
                 for (int b = 0; b < BT; ++b) inv[b] = 1.f;
-                if (d.xop == QDQ_X_RMSNORM) rms_scale<BT>(d, a.batch, cw, kCW, lane, red, inv);
-                stage_xb<BT>(d, tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf);
+                if (desc_xop(d) == QDQ_X_RMSNORM) rms_scale<BT>(d, a.ex[tl.g], a.batch, cw, kCW, lane, red, inv);
+                stage_xb<BT>(d, a.ex[tl.g], tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf);
                 named_bar_sync(kFlushBar, kCW * 32);
                 level_staged = true;
             }
@@ -1030,7 +1218,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 if (cw == 0)
                     for (int i = lane; i < tl.nrows; i += 32)
                         dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) |
-                                           ((tl.first_win && d.yop == QDQ_Y_STORE) ? 0u : 1u) | (d.amax ? 2u : 0u),
+                                           ((tl.first_win && desc_yop(d) == QDQ_Y_STORE) ? 0u : 1u) |
+                                               (desc_amax(d) ? 2u : 0u),
                         dstride[rg_base + i] = (int)d.rows;
                 if constexpr (BT == 1) {  // batch 1 adds every unit into the warp's column
                     for (int i = lane; i < tl.nrows; i += 32) mypart[rg_base + i] = 0.f;
@@ -1123,9 +1312,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-template <int BT, int MAXD, int MAXL>
+template <int BT, int MAXD, int MAXL, bool ATTN = false>
 static int launch1(const void *args, int grid, bool cooperative, cudaStream_t stream) {
-    auto kern = s1::stream1_kernel<BT, MAXD, MAXL>;
+    auto kern = s1::stream1_kernel<BT, MAXD, MAXL, ATTN>;
     constexpr int smem = s1::Smem<BT, MAXD>::kBytes;
     RelaxedCaptureScope relaxed;  // the first launch sets the kernel's attributes
     static bool attr_done[64] = {};
@@ -1157,7 +1346,10 @@ static int launch1_bt(const void *args, bool big, bool cooperative, int grid, cu
                : launch1<BT, kMaxGroupDescs, 1>(args, grid, cooperative, stream);
 }
 
-int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, cudaStream_t stream) {
+int stream1_launch(const void *args, bool big, bool cooperative, int grid, int bt, bool attn, cudaStream_t stream) {
+    if (attn)  // attention levels: batch 1, plan-sized arguments
+        return bt == 1 && big ? launch1<1, kMaxPlanDescs, kMaxPlanLevels, true>(args, grid, cooperative, stream)
+                              : QDQ_ERR_LIMIT;
     switch (bt) {
         case 1: return launch1_bt<1>(args, big, cooperative, grid, stream);
         case 2: return launch1_bt<2>(args, big, cooperative, grid, stream);

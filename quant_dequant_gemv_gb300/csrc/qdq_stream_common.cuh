@@ -20,17 +20,33 @@ struct DevDesc {
     int32_t cols;
     int32_t type;
     int32_t rb;     // bytes per row
-    int32_t pad0;   // keeps the fields below at the offsets the kernel's register allocation was tuned with
+    // step glue fused into the GEMV (plans only; zero elsewhere): bits 0-3 the x
+    // the dot product reads (QDQ_X_*), bits 4-7 how y is written (QDQ_Y_*), bit 8
+    // whether the rows take part in the plan's argmax; the operands are in DescEx
+    int32_t ops;
     int32_t kinds;  // bit k: the level's x needs swizzled copy kind k (0 plain, 2 q4_0-scaled)
-    int32_t pad1;
-    // step glue fused into the GEMV (plans only; zero elsewhere): the x the
-    // dot product reads (QDQ_X_*), how y is written (QDQ_Y_*), and whether the
-    // rows take part in the plan's argmax
-    const float *x2;  // QDQ_X_SWIGLU: the up input
-    const float *nw;  // QDQ_X_RMSNORM: the norm weights
-    float eps;
-    int32_t xop, yop, amax;
+    int32_t nkv;    // attention: KV heads
 };
+QDQ_DEV int desc_xop(const DevDesc &d) { return d.ops & 15; }
+QDQ_DEV int desc_yop(const DevDesc &d) { return (d.ops >> 4) & 15; }
+QDQ_DEV bool desc_amax(const DevDesc &d) { return (d.ops >> 8) & 1; }
+
+// Operands of the fused glue and of attention levels, apart from DevDesc so that
+// the descriptor the tile walk copies stays small.
+struct DescEx {
+    const float *x2;  // QDQ_X_SWIGLU: the up input (attention: k)
+    const float *nw;  // QDQ_X_RMSNORM: the norm weights (attention: v)
+    // attention (type kTypeAttn; x = q, y = the output, rows = query heads, cols =
+    // head_dim): the fp16 key / value caches [max_seq][nkv * head_dim]
+    uint16_t *kc, *vc;
+    float eps;
+    int32_t pad;
+};
+
+// A plan level that is not a GEMV: the attention block of one position (RoPE,
+// fp16 cache append, GQA online softmax), one query head per CTA.
+constexpr int kTypeAttn = kPlanAttnType;
+constexpr int kMaxRopePairs = 128;
 
 template <int MAXD, int MAXL>
 struct StreamArgs {
@@ -45,6 +61,10 @@ struct StreamArgs {
     long long *amax_out;
     int32_t level_start[MAXL + 1];
     DevDesc d[MAXD];
+    DescEx ex[MAXD];
+    // attention levels: the position and the pair frequencies base^(-2i/head_dim)
+    int32_t attn_pos, pad3;
+    double rope_f[kMaxRopePairs];
 };
 
 // ---------------------------------------------------------------------------
