@@ -36,6 +36,10 @@
  *   q8_0, q4_0      pinned: hand-built blocks with closed-form values. The q4_0
  *                   nibble order (low nibble = weight i, high = weight i+16) is
  *                   the workload definition's reading.
+ *   Q5_0, Q5_1,     layouts not on the pages (ggml's, a reading): pinned by
+ *   ggml q8_0, Q2_K hand-built blocks and mutations; Q2_K also by the page's 84
+ *                   bytes per 256 weights. "Parity unpinned" against the pages
+ *                   for the bit placements.
  *   GEMV            pinned: exact rational sums on tiny inputs, unit-vector
  *                   columns (catches a transposed operand), closed forms.
  */
@@ -43,7 +47,8 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_Q4_0 = 1, ORC_Q8_0 = 2, ORC_Q4_K = 3, ORC_Q6_K = 4 };
+enum { ORC_Q4_0 = 1, ORC_Q8_0 = 2, ORC_Q4_K = 3, ORC_Q6_K = 4, ORC_Q5_0 = 5, ORC_Q5_1 = 6, ORC_Q8_0G = 7,
+       ORC_Q2_K = 8 };
 
 /* ---- IEEE-754 binary16 -> binary32, from the format definition ---------------
  * sign s (1 bit), exponent e (5 bits, bias 15), fraction f (10 bits):
@@ -152,20 +157,81 @@ void orc_dequant_q4_0_block(const uint8_t *blk, float *out) {
     }
 }
 
+/* ---- More GGUF formats [S21 section 2: "eight formats", Q2_K 84 bytes per 256;
+ * the layouts themselves are not on the pages] -----------------------------------
+ * These follow the published ggml block layouts (a reading; pinned against the
+ * pages only by Q2_K's 84 bytes per 256 weights, and by hand-built blocks).
+ *
+ * Q5_0: 22 bytes -> 32 weights: fp16 d; qh, four bytes read as a little-endian
+ * 32-bit word whose bit i is the fifth bit of weight i; 16 bytes qs, byte i
+ * holding weight i in its low nibble and weight i+16 in its high nibble.
+ * q = nibble | bit << 4 (0..31); w = (q - 16) * d (one rounding).               */
+static int q5_quant(const uint8_t *qh4, const uint8_t *qs, int i) {
+    uint32_t qh = (uint32_t)qh4[0] | ((uint32_t)qh4[1] << 8) | ((uint32_t)qh4[2] << 16) | ((uint32_t)qh4[3] << 24);
+    int nib = (i < 16) ? (qs[i] & 15) : (qs[i - 16] >> 4);
+    return nib | (int)(((qh >> i) & 1u) << 4);
+}
+
+void orc_dequant_q5_0_block(const uint8_t *blk, float *out) {
+    float d = rd_fp16(blk);
+    for (int i = 0; i < 32; ++i) out[i] = (float)(q5_quant(blk + 2, blk + 6, i) - 16) * d;
+}
+
+/* Q5_1: 24 bytes: fp16 d, fp16 m, qh, qs as Q5_0; w = q * d + m (q * d is exact
+ * in binary32, so this is one rounding).                                         */
+void orc_dequant_q5_1_block(const uint8_t *blk, float *out) {
+    float d = rd_fp16(blk), m = rd_fp16(blk + 2);
+    for (int i = 0; i < 32; ++i) {
+        float a = (float)q5_quant(blk + 4, blk + 8, i) * d;
+        out[i] = a + m;
+    }
+}
+
+/* ggml q8_0: 34 bytes: fp16 d, 32 int8 q; w = q * d. (PETIT's q8_0 has an fp32
+ * scale instead.)                                                                */
+void orc_dequant_q8_0g_block(const uint8_t *blk, float *out) {
+    float d = rd_fp16(blk);
+    const int8_t *q = (const int8_t *)(blk + 2);
+    for (int i = 0; i < 32; ++i) out[i] = (float)q[i] * d;
+}
+
+/* Q2_K: 84 bytes -> 256 weights: 16 scale bytes (low nibble: scale, high nibble:
+ * min, one pair per 16 weights), 64 bytes of 2-bit quants, fp16 d, fp16 dmin.
+ * Element e = 128n + 32j + l (n = half, j = 0..3, l = 0..31): q = bits 2j..2j+1
+ * of qs[32n + l]; its pair is scales[8n + 2j + l/16].
+ * Value, left to right: (d * sc) * q - (dmin * mn).                              */
+void orc_dequant_q2_K_block(const uint8_t *blk, float *out) {
+    const uint8_t *scales = blk, *qs = blk + 16;
+    float d = rd_fp16(blk + 80), dmin = rd_fp16(blk + 82);
+    for (int e = 0; e < 256; ++e) {
+        int n = e / 128, j = (e % 128) / 32, l = e % 32;
+        int q = (qs[32 * n + l] >> (2 * j)) & 3;
+        int sm = scales[8 * n + 2 * j + l / 16];
+        float a = d * (float)(sm & 15);
+        a = a * (float)q;
+        float b = dmin * (float)(sm >> 4);
+        out[e] = a - b;
+    }
+}
+
 int orc_block_bytes(int type) {
     switch (type) {
     case ORC_Q4_0: return 18;
     case ORC_Q8_0: return 36;
     case ORC_Q4_K: return 144;
     case ORC_Q6_K: return 210;
+    case ORC_Q5_0: return 22;
+    case ORC_Q5_1: return 24;
+    case ORC_Q8_0G: return 34;
+    case ORC_Q2_K: return 84;
     default: return -1;
     }
 }
 
 int orc_block_weights(int type) {
     switch (type) {
-    case ORC_Q4_0: case ORC_Q8_0: return 32;
-    case ORC_Q4_K: case ORC_Q6_K: return 256;
+    case ORC_Q4_0: case ORC_Q8_0: case ORC_Q5_0: case ORC_Q5_1: case ORC_Q8_0G: return 32;
+    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q2_K: return 256;
     default: return -1;
     }
 }
@@ -183,6 +249,10 @@ int orc_dequant(int type, const uint8_t *blocks, int64_t n, float *out) {
         case ORC_Q6_K: orc_dequant_q6_K_block(blk, o); break;
         case ORC_Q8_0: orc_dequant_q8_0_block(blk, o); break;
         case ORC_Q4_0: orc_dequant_q4_0_block(blk, o); break;
+        case ORC_Q5_0: orc_dequant_q5_0_block(blk, o); break;
+        case ORC_Q5_1: orc_dequant_q5_1_block(blk, o); break;
+        case ORC_Q8_0G: orc_dequant_q8_0g_block(blk, o); break;
+        case ORC_Q2_K: orc_dequant_q2_K_block(blk, o); break;
         }
     }
     return 0;

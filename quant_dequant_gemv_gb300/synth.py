@@ -32,10 +32,17 @@ Q4_0 = 1
 Q8_0 = 2  # PETIT q8_0: fp32 scale + 32 int8
 Q4_K = 3
 Q6_K = 4
+# More GGUF block formats (ggml layouts): Q5_0 (22 B / 32), Q5_1 (24 B / 32),
+# ggml's q8_0 with an fp16 scale (34 B / 32), Q2_K (84 B / 256).
+Q5_0 = 5
+Q5_1 = 6
+Q8_0G = 7
+Q2_K = 8
 
-TYPE_NAMES = {Q4_0: "q4_0", Q8_0: "q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K"}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210}
-BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256}
+TYPE_NAMES = {Q4_0: "q4_0", Q8_0: "q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q5_0: "Q5_0", Q5_1: "Q5_1",
+              Q8_0G: "q8_0 (ggml)", Q2_K: "Q2_K"}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210, Q5_0: 22, Q5_1: 24, Q8_0G: 34, Q2_K: 84}
+BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_0: 32, Q5_1: 32, Q8_0G: 32, Q2_K: 256}
 
 SCALE_LO, SCALE_HI = 1e-4, 1e-2
 
@@ -66,10 +73,19 @@ def gen_blocks(qtype: int, nblocks: int, rng: np.random.Generator) -> np.ndarray
         d = rng.uniform(SCALE_LO, SCALE_HI, nblocks).astype("<f4")
         out[:, 0:4] = d.view(np.uint8).reshape(-1, 4)
         out[:, 4:36] = rng.integers(-127, 128, (nblocks, 32)).astype(np.int8).view(np.uint8)
-    elif qtype == Q4_0:
+    elif qtype in (Q4_0, Q5_0, Q8_0G):  # fp16 d, then quant bytes
         d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
         out[:, 0:2] = _fp16_bytes(d)
-        out[:, 2:18] = rng.integers(0, 256, (nblocks, 16), dtype=np.uint8)
+        out[:, 2:bb] = rng.integers(0, 256, (nblocks, bb - 2), dtype=np.uint8)
+    elif qtype == Q5_1:  # fp16 d, fp16 m (a negative offset of the range), quant bytes
+        d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
+        out[:, 0:2] = _fp16_bytes(d)
+        out[:, 2:4] = _fp16_bytes(-16 * d * rng.uniform(0.5, 1.5, nblocks))
+        out[:, 4:24] = rng.integers(0, 256, (nblocks, 20), dtype=np.uint8)
+    elif qtype == Q2_K:  # scale/min nibbles and 2-bit quants, then fp16 d, dmin
+        out[:, 0:80] = rng.integers(0, 256, (nblocks, 80), dtype=np.uint8)
+        out[:, 80:82] = _fp16_bytes(rng.uniform(SCALE_LO, SCALE_HI, nblocks))
+        out[:, 82:84] = _fp16_bytes(rng.uniform(SCALE_LO, SCALE_HI, nblocks))
     else:
         raise ValueError(f"unknown block type {qtype}")
     return out.reshape(-1)
@@ -98,8 +114,14 @@ def gen_blocks_full_range(qtype: int, nblocks: int, rng: np.random.Generator) ->
         clamp_fp16(2)
     elif qtype == Q6_K:
         clamp_fp16(208)
-    elif qtype == Q4_0:
+    elif qtype in (Q4_0, Q5_0, Q8_0G):
         clamp_fp16(0)
+    elif qtype == Q5_1:
+        clamp_fp16(0)
+        clamp_fp16(2)
+    elif qtype == Q2_K:
+        clamp_fp16(80)
+        clamp_fp16(82)
     elif qtype == Q8_0:
         w = out[:, 0:4].copy().view("<u4").reshape(-1)
         e = (w >> 23) & 0xFF
