@@ -50,13 +50,20 @@ WORKLOADS = {
     "token": "1.1B Llama-shape token step, batch 1, greedy decode: embedding row, 22 layers of rmsnorm -> "
              "q/k/v -> RoPE + fp16 KV cache + GQA attention -> o + residual -> rmsnorm -> gate/up -> SwiGLU -> "
              "down + residual, final rmsnorm -> output head + argmax (Q4_K_M mix, 667,152,384 GEMV weight bytes)",
+    "ffn_q5_0": "Q5_0 GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
+    "ffn_q5_1": "Q5_1 GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
+    "ffn_q8_0g": "ggml q8_0 (fp16 scale) GEMV 5632x2048 (ffn_gate/up shape)",
+    "ffn_q2k": "Q2_K GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
     "dequant_q4k": "standalone dequantisation, Q4_K, 2^27 weights -> fp32",
     "dequant_q6k": "standalone dequantisation, Q6_K, 2^27 weights -> fp32",
     "dequant_q8_0": "standalone dequantisation, PETIT q8_0, 2^27 weights -> fp32",
     "dequant_q4_0": "standalone dequantisation, PETIT q4_0, 2^27 weights -> fp32",
+    "dequant_q5_1": "standalone dequantisation, Q5_1 (ggml layout), 2^27 weights -> fp32",
+    "dequant_q2k": "standalone dequantisation, Q2_K (ggml layout), 2^27 weights -> fp32",
 }
+MORE_GEMV = {"ffn_q5_0": synth.Q5_0, "ffn_q5_1": synth.Q5_1, "ffn_q8_0g": synth.Q8_0G, "ffn_q2k": synth.Q2_K}
 DEQUANT_TYPES = {"dequant_q4k": synth.Q4_K, "dequant_q6k": synth.Q6_K, "dequant_q8_0": synth.Q8_0,
-                 "dequant_q4_0": synth.Q4_0}
+                 "dequant_q4_0": synth.Q4_0, "dequant_q5_1": synth.Q5_1, "dequant_q2k": synth.Q2_K}
 DEQUANT_N = 1 << 27  # weights per dequantisation step: in + out bytes are several times L2
 
 
@@ -75,6 +82,8 @@ def workload_levels(name: str, layers: int = 22) -> list[list[synth.Gemv]]:
         return [[synth.Gemv("ffn_gate", synth.Q4_K, 5632, 2048)]]
     if name == "ffn_q6k":
         return [[synth.Gemv("ffn_down", synth.Q6_K, 2048, 5632)]]
+    if name in MORE_GEMV:
+        return [[synth.Gemv("ffn_gate", MORE_GEMV[name], 5632, 2048)]]
     if name in ("q8_0", "q4_0"):
         t = synth.Q8_0 if name == "q8_0" else synth.Q4_0
         return [[synth.Gemv("w_up", t, 14336, 4096)], [synth.Gemv("w_down", t, 4096, 14336)]]
@@ -213,12 +222,16 @@ def build_inputs(levels, batch, device, seed=0):
 
 L2_BYTES = 129 * 2 ** 20   # GB300 L2
 def mma_min_batch(qtype):  # single GEMVs from this batch on run on the tensor cores (library dispatch)
+    if qtype in MORE_GEMV.values():
+        return 1 << 30  # the further formats always run gemv_more_kernel
     return 4 if qtype in (synth.Q8_0, synth.Q4_0) else 5
 GROUP = 8                  # single-GEMV workloads: steps per replayed CUDA graph
 
 
 def gemv_launches(g, batch):
     """Kernel launches of one qdq_gemv call (mirrors the library's dispatch)."""
+    if g.qtype in MORE_GEMV.values():
+        return (batch + 7) // 8  # gemv_more_kernel per slice of at most 8 columns
     if batch < mma_min_batch(g.qtype):
         return 1
     per = 32 if g.qtype == synth.Q6_K else 64
@@ -765,6 +778,8 @@ def main():
                                     else "dequant_kernel" if args.workload in DEQUANT_TYPES
                                     else "mma_gemv_kernel (tensor cores)"
                                     if args.batch >= mma_min_batch(levels[0][0].qtype)
+                                    else "gemv_more_kernel (exact per-weight decode)"
+                                    if args.workload in MORE_GEMV
                                     else "stream1_kernel (one GEMV per launch)")},
             "e2e": {"value": round(world * abytes / e2e_s / 1e9, 2), "unit": "GB/s", "tok_s": round(world / e2e_s, 1),
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

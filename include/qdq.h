@@ -17,6 +17,22 @@
  *   QDQ_Q4_0  PETIT q4_0, 18 bytes per 32 weights (same section): fp16 scale d,
  *             16 bytes; byte i holds weight i (low nibble) and weight i+16 (high
  *             nibble). w = (q-8)*d.
+ *   More GGUF formats. The pages name eight GGUF formats and give Q2_K's size
+ *   (84 bytes per 256 weights, "S21 The Capstone: picoLM, in Python", section
+ *   2); the layouts follow the published ggml block layouts:
+ *   QDQ_Q5_0       22 bytes per 32: fp16 d; qh (4 bytes, little-endian word, bit
+ *                  i = fifth bit of weight i); 16 nibble bytes as q4_0.
+ *                  w = (q-16)*d, q = nibble | bit << 4.
+ *   QDQ_Q5_1       24 bytes per 32: fp16 d, fp16 m, qh, 16 nibble bytes.
+ *                  w = q*d + m.
+ *   QDQ_Q8_0_GGML  34 bytes per 32: fp16 d, 32 int8. w = q*d.
+ *   QDQ_Q2_K       84 bytes per 256: 16 bytes of (scale | min << 4) per 16
+ *                  weights, 64 bytes of 2-bit quants (weight 128n + 32j + l: bits
+ *                  2j..2j+1 of byte 32n + l, pair 8n + 2j + l/16), fp16 d, fp16
+ *                  dmin. w = d*sc*q - dmin*mn.
+ *   These four are decoded by qdq_dequant and multiplied by qdq_gemv (a
+ *   separate exact-per-weight kernel, any batch); groups and plans take the
+ *   main four only (QDQ_ERR_TYPE).
  *
  * Conventions for every call:
  *   - Pointers named W, blocks, x, y, out are DEVICE pointers (cudaMalloc'd or
@@ -49,7 +65,11 @@ extern "C" {
 
 typedef struct CUstream_st *qdq_stream_t; /* == cudaStream_t */
 
-enum qdq_type { QDQ_Q4_0 = 1, QDQ_Q8_0 = 2, QDQ_Q4_K = 3, QDQ_Q6_K = 4 };
+enum qdq_type {
+    QDQ_Q4_0 = 1, QDQ_Q8_0 = 2, QDQ_Q4_K = 3, QDQ_Q6_K = 4,
+    /* More GGUF formats (see the notes below the main four): */
+    QDQ_Q5_0 = 5, QDQ_Q5_1 = 6, QDQ_Q8_0_GGML = 7, QDQ_Q2_K = 8
+};
 
 enum qdq_status {
     QDQ_OK = 0,
@@ -303,6 +323,7 @@ int qdq_quantize(int type, const float *x, int64_t n, void *blocks, qdq_stream_t
  * qdq_gguf_parse fills up to max_tensors entries (QDQ_ERR_LIMIT if the file has
  * more) with the tensors' names, dims (dims[0] innermost: the row length),
  * GGUF type code, the library type that decodes it (QDQ_Q4_0 for type 2,
+ * QDQ_Q5_0 for 6, QDQ_Q5_1 for 7, QDQ_Q8_0_GGML for 8, QDQ_Q2_K for 10,
  * QDQ_Q4_K for 12, QDQ_Q6_K for 14, else 0), absolute byte offset and size.
  * qdq_gguf_find_kv locates a metadata value: its GGUF value type and the byte
  * offset of the value (QDQ_ERR_NOT_FOUND if the key is absent).

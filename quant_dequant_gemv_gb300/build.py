@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 BUILD = Path(os.environ.get("QDQ_BUILD_DIR", PKG / "_build"))
 LIB = BUILD / "libqdq.so"
 SOURCES = ["qdq_api.cu", "qdq_dequant.cu", "qdq_stream.cu", "qdq_stream1.cu", "qdq_mma.cu", "qdq_noalloc.cu",
-           "qdq_llama.cu", "qdq_quantize.cu"]
+           "qdq_llama.cu", "qdq_quantize.cu", "qdq_gemv_more.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               f"-I{INCLUDE}", f"-I{CSRC}"] + os.environ.get("QDQ_EXTRA_NVCC_FLAGS", "").split()

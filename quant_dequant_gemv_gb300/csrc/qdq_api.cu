@@ -6,6 +6,7 @@
 #include <new>
 #include <vector>
 
+#include "qdq_decode.cuh"
 #include "qdq_internal.h"
 
 namespace qdq {
@@ -41,9 +42,11 @@ const DeviceInfo &current_device(int *status) {
     return d;
 }
 
-static int check_type(int type) {
-    return (type == QDQ_Q4_0 || type == QDQ_Q8_0 || type == QDQ_Q4_K || type == QDQ_Q6_K) ? QDQ_OK : QDQ_ERR_TYPE;
+// The main four formats (every path) and the further GGUF ones (dequant, qdq_gemv).
+static bool main_type(int type) {
+    return type == QDQ_Q4_0 || type == QDQ_Q8_0 || type == QDQ_Q4_K || type == QDQ_Q6_K;
 }
+static int check_type(int type) { return (main_type(type) || is_more_type(type)) ? QDQ_OK : QDQ_ERR_TYPE; }
 
 // Device (or managed) memory of the current device, 16-byte aligned.
 static int check_dev_ptr(const void *p, int device) {
@@ -79,6 +82,7 @@ static int check_gemv_ptrs(const void *W, const float *x, float *y, int device) 
 int check_descs(const qdq_gemv_desc *descs, int n, int batch, int device) {
     if (descs == nullptr || n < 0) return QDQ_ERR_PTR;
     for (int i = 0; i < n; ++i) {
+        if (!main_type(descs[i].type)) return QDQ_ERR_TYPE;  // groups and plans: the main four
         int rc = check_gemv_shape(descs[i].type, descs[i].rows, descs[i].cols, batch);
         if (rc) return rc;
         if (descs[i].rows == 0 || descs[i].cols == 0) return QDQ_ERR_SHAPE;
@@ -117,25 +121,9 @@ struct qdq_plan {
 
 extern "C" {
 
-int qdq_block_bytes(int type) {
-    switch (type) {
-        case QDQ_Q4_0: return 18;
-        case QDQ_Q8_0: return 36;
-        case QDQ_Q4_K: return 144;
-        case QDQ_Q6_K: return 210;
-        default: return -1;
-    }
-}
+int qdq_block_bytes(int type) { return check_type(type) ? -1 : fmt_bytes(type); }
 
-int qdq_block_weights(int type) {
-    switch (type) {
-        case QDQ_Q4_0:
-        case QDQ_Q8_0: return 32;
-        case QDQ_Q4_K:
-        case QDQ_Q6_K: return 256;
-        default: return -1;
-    }
-}
+int qdq_block_weights(int type) { return check_type(type) ? -1 : fmt_weights(type); }
 
 const char *qdq_status_string(int status) {
     switch (status) {
@@ -195,6 +183,7 @@ int qdq_gemv(int type, const void *W, int64_t rows, int64_t cols, const float *x
     cudaStream_t s = (cudaStream_t)stream;
     if (cols == 0)
         return cudaMemsetAsync(y, 0, (size_t)batch * rows * sizeof(float), s) == cudaSuccess ? QDQ_OK : QDQ_ERR_CUDA;
+    if (is_more_type(type)) return launch_gemv_more(type, W, rows, cols, x, y, batch, s, dev.sm_count);
     if (batch >= mma_min_batch(type)) {
         rc = launch_mma_gemv(type, W, rows, cols, x, y, batch, s, dev.sm_count);
         if (rc != QDQ_ERR_LIMIT) return rc;

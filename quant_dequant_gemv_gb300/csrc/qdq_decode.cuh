@@ -107,6 +107,15 @@ QDQ_DEV uint32_t ldg_u32(const uint8_t *p) { return __ldg((const unsigned int *)
 // 4 bytes at a 2-byte-aligned address
 QDQ_DEV uint32_t ldg_u32_a2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p + 2) << 16); }
 
+// Block geometry of every format the decoder knows.
+__host__ __device__ constexpr int fmt_bytes(int t) {
+    return t == QDQ_Q4_K ? 144 : t == QDQ_Q6_K ? 210 : t == QDQ_Q8_0 ? 36 : t == QDQ_Q4_0 ? 18 : t == QDQ_Q5_0 ? 22
+           : t == QDQ_Q5_1 ? 24 : t == QDQ_Q8_0_GGML ? 34 : t == QDQ_Q2_K ? 84 : 0;
+}
+__host__ __device__ constexpr int fmt_weights(int t) {
+    return (t == QDQ_Q4_K || t == QDQ_Q6_K || t == QDQ_Q2_K) ? 256 : 32;
+}
+
 // Weights e0 .. e0+3 (e0 a multiple of 4) of the block at `blk`.
 template <int TYPE>
 QDQ_DEV float4 decode4(const uint8_t *blk, int e0) {
@@ -144,6 +153,43 @@ QDQ_DEV float4 decode4(const uint8_t *blk, int e0) {
         v.y = q8_0_weight(d, (int)(int8_t)((q >> 8) & 0xFF));
         v.z = q8_0_weight(d, (int)(int8_t)((q >> 16) & 0xFF));
         v.w = q8_0_weight(d, (int)(int8_t)(q >> 24));
+    } else if constexpr (TYPE == QDQ_Q5_0 || TYPE == QDQ_Q5_1) {  // blk 2-byte aligned
+        // q = nibble | fifth bit << 4; Q5_0: (q - 16) * d; Q5_1: q * d + m (q * d exact)
+        constexpr int kQh = TYPE == QDQ_Q5_0 ? 2 : 4;
+        const float d = half_bits_to_float(ldg_u16(blk));
+        const float m = TYPE == QDQ_Q5_1 ? half_bits_to_float(ldg_u16(blk + 2)) : 0.0f;
+        const uint32_t qh = ldg_u32_a2(blk + kQh) >> e0;
+        uint32_t q = ldg_u32_a2(blk + kQh + 4 + (e0 & 15));
+        if (e0 >= 16) q >>= 4;
+        float w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int qq = (int)(((q >> (8 * k)) & 15) | (((qh >> k) & 1) << 4));
+            if constexpr (TYPE == QDQ_Q5_0)
+                w[k] = __fmul_rn((float)(qq - 16), d);
+            else
+                w[k] = __fadd_rn(__fmul_rn((float)qq, d), m);
+        }
+        v = make_float4(w[0], w[1], w[2], w[3]);
+    } else if constexpr (TYPE == QDQ_Q8_0_GGML) {  // blk 2-byte aligned
+        const float d = half_bits_to_float(ldg_u16(blk));
+        const uint32_t q = ldg_u32_a2(blk + 2 + e0);
+        v.x = __fmul_rn((float)(int)(int8_t)(q & 0xFF), d);
+        v.y = __fmul_rn((float)(int)(int8_t)((q >> 8) & 0xFF), d);
+        v.z = __fmul_rn((float)(int)(int8_t)((q >> 16) & 0xFF), d);
+        v.w = __fmul_rn((float)(int)(int8_t)(q >> 24), d);
+    } else if constexpr (TYPE == QDQ_Q2_K) {  // blk 4-byte aligned
+        // weight 128n + 32j + l: bits 2j..2j+1 of qs[32n + l], pair 8n + 2j + l/16;
+        // (d * sc) * q - (dmin * mn), evaluated left to right
+        const int n = e0 >> 7, j = (e0 >> 5) & 3, l = e0 & 31;
+        const uint32_t q = ldg_u32(blk + 16 + 32 * n + l) >> (2 * j);
+        const uint32_t sm = __ldg(blk + 8 * n + 2 * j + (l >> 4));
+        const float dl = __fmul_rn(half_bits_to_float(ldg_u16(blk + 80)), (float)(sm & 15));
+        const float ml = __fmul_rn(half_bits_to_float(ldg_u16(blk + 82)), (float)(sm >> 4));
+        v.x = __fsub_rn(__fmul_rn(dl, (float)(q & 3)), ml);
+        v.y = __fsub_rn(__fmul_rn(dl, (float)((q >> 8) & 3)), ml);
+        v.z = __fsub_rn(__fmul_rn(dl, (float)((q >> 16) & 3)), ml);
+        v.w = __fsub_rn(__fmul_rn(dl, (float)((q >> 24) & 3)), ml);
     } else {  // QDQ_Q4_0, blk 2-byte aligned
         const float d = half_bits_to_float(ldg_u16(blk));
         uint32_t q = ldg_u32_a2(blk + 2 + (e0 & 15));

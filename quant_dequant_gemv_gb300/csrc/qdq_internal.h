@@ -24,6 +24,10 @@ int check_levels(const int *level, int n, int max_levels, int *nlevels);
 
 int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStream_t stream, int sm_count);
 int launch_quantize(int type, const float *x, int64_t n, void *blocks, cudaStream_t stream, int sm_count);
+// The further GGUF formats (Q5_0, Q5_1, ggml q8_0, Q2_K): qdq_gemv_more.cu.
+bool is_more_type(int type);
+int launch_gemv_more(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y, int batch,
+                     cudaStream_t stream, int sm_count);
 
 // The streaming (CUDA-core) GEMV over a list of GEMVs grouped in dependency levels.
 struct StreamPlanHost;  // opaque: the packed kernel arguments

@@ -149,10 +149,10 @@ void ggml_geometry(uint32_t t, int *bb, int *bw, int *qdq_type) {
         case 1: *bb = 2, *bw = 1; break;                             // f16
         case 2: *bb = 18, *bw = 32, *qdq_type = QDQ_Q4_0; break;     // q4_0: fp16 d + 16 nibble bytes
         case 3: *bb = 20, *bw = 32; break;                           // q4_1
-        case 6: *bb = 22, *bw = 32; break;                           // q5_0
-        case 7: *bb = 24, *bw = 32; break;                           // q5_1
-        case 8: *bb = 34, *bw = 32; break;                           // ggml q8_0 (fp16 scale)
-        case 10: *bb = 84, *bw = 256; break;                         // q2_K
+        case 6: *bb = 22, *bw = 32, *qdq_type = QDQ_Q5_0; break;     // q5_0
+        case 7: *bb = 24, *bw = 32, *qdq_type = QDQ_Q5_1; break;     // q5_1
+        case 8: *bb = 34, *bw = 32, *qdq_type = QDQ_Q8_0_GGML; break;  // ggml q8_0 (fp16 scale)
+        case 10: *bb = 84, *bw = 256, *qdq_type = QDQ_Q2_K; break;   // q2_K
         case 11: *bb = 110, *bw = 256; break;                        // q3_K
         case 12: *bb = 144, *bw = 256, *qdq_type = QDQ_Q4_K; break;  // q4_K
         case 13: *bb = 176, *bw = 256; break;                        // q5_K

@@ -34,6 +34,9 @@ def test_every_declared_function_is_exported(lib):
 def test_block_geometry(lib):
     assert [lib.qdq_block_bytes(t) for t in (1, 2, 3, 4)] == [18, 36, 144, 210]
     assert [lib.qdq_block_weights(t) for t in (1, 2, 3, 4)] == [32, 32, 256, 256]
+    # Q5_0, Q5_1, ggml q8_0, Q2_K (84 bytes per 256: the page's figure)
+    assert [lib.qdq_block_bytes(t) for t in (5, 6, 7, 8)] == [22, 24, 34, 84]
+    assert [lib.qdq_block_weights(t) for t in (5, 6, 7, 8)] == [32, 32, 32, 256]
     assert lib.qdq_block_bytes(0) == -1 and lib.qdq_block_weights(99) == -1
 
 
@@ -46,7 +49,7 @@ def test_status_strings(lib):
 
 def test_argument_checks_precede_device_work(lib):
     # These return before the library touches a device, so they hold on any host.
-    assert lib.qdq_gemv(7, 0, 4, 256, 0, 0, 1, 0) == -1            # type
+    assert lib.qdq_gemv(99, 0, 4, 256, 0, 0, 1, 0) == -1           # type
     assert lib.qdq_gemv(3, 0, 4, 100, 0, 0, 1, 0) == -2            # cols % 256
     assert lib.qdq_gemv(3, 0, -1, 256, 0, 0, 1, 0) == -2           # rows < 0
     assert lib.qdq_gemv(3, 0, 4, 256, 0, 0, 0, 0) == -2            # batch < 1
