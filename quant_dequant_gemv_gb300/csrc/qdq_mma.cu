@@ -705,10 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kWarpMma) {
         // ---- MMA issue: the whole warp runs the loop with warp-uniform operands and
-        // one elected lane issues a sub-chunk's MMAs in one go, so the descriptors
-        // stay in uniform registers (a lone thread issuing from per-thread registers
-        // reaches a tenth of the rate). The two commits follow in their own elected
-        // block after a warp barrier.
+        // one elected lane issues a sub-chunk's MMAs and its two commits in one go,
+        // so the descriptors stay in uniform registers (a lone thread issuing from
+        // per-thread registers reaches a tenth of the rate).
         // Per K-step t of a sub-chunk: Z_g += q x_hi and Z_g += q x_lo into the
         // accumulator region of t's group.
         const uint32_t idesc = make_idesc(b_pad), idesc2 = make_idesc(2 * b_pad);
@@ -727,7 +726,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0 && j < 8) MTC(7, 16 + j);
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(a_full + 8 * s, phase, status));
                     if (lane == 0) MTC(5, j);
-                    if (ok && j >= nd) ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_empty + 8 * rd_s, rd_p ^ 1, status));
+                    // In four-group mode the set's release needs no wait of its own: group
+                    // G releases set j - 4 (the set of j: nd is 4) after its epilogue and
+                    // before it decodes sub-chunk j, and the A stage of j is full only
+                    // after that decode (its tensor-memory reads are fenced before both
+                    // arrivals, in program order).
+                    if (!rr_groups(TYPE, BP) && ok && j >= nd)
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(d_empty + 8 * rd_s, rd_p ^ 1, status));
                     if (lane == 0) MTC(6, j);
                     if (ok) {
                         tc_fence_after();
@@ -749,10 +754,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     }
                                 }
                             }
-                        }
-                        __syncwarp();
-                        if (lane == 0 && j < 8) MTC(7, 32 + j);
-                        if (elect_one()) {
                             mma_commit(a_empty + 8 * s);
                             mma_commit(d_full + 8 * rd_s);
                         }
