@@ -71,22 +71,41 @@ float orc_fp16_to_fp32(uint16_t h) {
 static float rd_fp16(const uint8_t *p) { return orc_fp16_to_fp32((uint16_t)(p[0] | (p[1] << 8))); }
 
 /* ---- Q4_K: 144 bytes -> 256 weights [S21 section 2] ----------------------------
- * bytes 0-1 fp16 d, 2-3 fp16 dmin, 4-15 the packed 6-bit scale/min fields,
- * 16-143 the nibbles. Field j of the eight (sub-block j, 32 weights each):
- *   j < 4 : the field sits in the low six bits of its own byte:
- *           sc = p[j] & 63,            mn = p[j+4] & 63
- *   j >= 4: low four bits from p[j+4], top two bits from bits 6-7 of an earlier
- *           byte:
- *           sc = (p[j+4] & 15) | (p[j-4] >> 6) << 4
- *           mn = (p[j+4] >> 4) | (p[j]   >> 6) << 4                            */
-void orc_q4k_scale_min(const uint8_t *p, int j, int *sc, int *mn) {
+ * bytes 0-1 fp16 d, 2-3 fp16 dmin, 4-15 (p[0..11] below) eight 6-bit scales and
+ * eight 6-bit mins, one pair per 32-weight sub-block, bit-packed (the page's
+ * super-block diagram: 12 bytes of packed 6-bit scales and mins; fields 4-7
+ * straddle byte boundaries).
+ * Where bit b of field j of kind k (k = 0: scale, 1: min) lives in p:
+ *   fields 0-3 sit whole in the low six bits of one byte: scales in bytes 0-3,
+ *     mins in bytes 4-7 (byte 4k + j, bit b);
+ *   fields 4-7 keep their four low bits in byte j+4, scales in its low nibble
+ *     and mins in its high nibble (bit 4k + b), and their two top bits in bits
+ *     6-7 of the byte that holds field j-4 of the same kind (byte 4k + j - 4,
+ *     bit 6 + b - 4).
+ * The value is assembled one bit at a time from those positions.               */
+static void q4k_field_bit(int k, int j, int b, int *byte, int *bit) {
     if (j < 4) {
-        *sc = p[j] & 63;
-        *mn = p[j + 4] & 63;
+        *byte = 4 * k + j;
+        *bit = b;
+    } else if (b < 4) {
+        *byte = j + 4;
+        *bit = 4 * k + b;
     } else {
-        *sc = (p[j + 4] & 15) | ((p[j - 4] >> 6) << 4);
-        *mn = (p[j + 4] >> 4) | ((p[j] >> 6) << 4);
+        *byte = 4 * k + (j - 4);
+        *bit = 6 + (b - 4);
     }
+}
+
+void orc_q4k_scale_min(const uint8_t *p, int j, int *sc, int *mn) {
+    int v[2] = {0, 0};
+    for (int k = 0; k < 2; ++k)
+        for (int b = 0; b < 6; ++b) {
+            int byte, bit;
+            q4k_field_bit(k, j, b, &byte, &bit);
+            v[k] |= ((p[byte] >> bit) & 1) << b;
+        }
+    *sc = v[0];
+    *mn = v[1];
 }
 
 /* The nibble bytes form four chunks of 32 bytes. In chunk c the low nibbles are

@@ -39,14 +39,15 @@ Q4K_PINS = [
 ]
 
 MUTANTS_Q4K = {
-    "scale top bits not shifted": ("((p[j - 4] >> 6) << 4)", "(p[j - 4] >> 6)"),
-    "min top bits from p[j-4]": ("| ((p[j] >> 6) << 4);", "| ((p[j - 4] >> 6) << 4);"),
-    "min low bits from low nibble": ("*mn = (p[j + 4] >> 4)", "*mn = (p[j + 4] & 15)"),
+    "top bits from bits 5-6": ("*bit = 6 + (b - 4);", "*bit = 5 + (b - 4);"),
+    "top bits from the byte of field j": ("*byte = 4 * k + (j - 4);", "*byte = 4 * k + j;"),
+    "min low bits from low nibble": ("*bit = 4 * k + b;", "*bit = b;"),
+    "low bits of fields 4-7 from byte j+3": ("*byte = j + 4;", "*byte = j + 3;"),
+    "fields read as 7 bits": ("for (int b = 0; b < 6; ++b) {", "for (int b = 0; b < 7; ++b) {"),
     "nibble halves swapped": ("(i < 32) ? (qs[32 * c + i] & 15) : (qs[32 * c + i - 32] >> 4)",
                               "(i < 32) ? (qs[32 * c + i] >> 4) : (qs[32 * c + i - 32] & 15)"),
     "low nibbles paired with odd sub-block": ("int s = 2 * c + (i >= 32);",
                                               "int s = 2 * c + (i < 32);"),
-    "j<4 mask keeps 7 bits": ("*sc = p[j] & 63;", "*sc = p[j] & 127;"),
     "dmin and d swapped": ("float d = rd_fp16(blk), dmin = rd_fp16(blk + 2);",
                            "float dmin = rd_fp16(blk), d = rd_fp16(blk + 2);"),
 }
