@@ -371,7 +371,7 @@ def test_errors_host_and_misaligned_pointers(q):
         q.gemv(synth.Q4_K, W, 1, 2000, x, y, 1)
     assert e.value.rc == -2
     with pytest.raises(QdqError) as e:
-        q.gemv(5, W, 1, 2048, x, y, 1)
+        q.gemv(99, W, 1, 2048, x, y, 1)  # no such type
     assert e.value.rc == -1
 
 
