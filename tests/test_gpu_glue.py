@@ -260,3 +260,35 @@ def test_token_step(q, norm_scale):
         assert np.all(err <= 1e-4 * S[0] + 1e-6), (pos, float(err.max()), float(S[0].max()))
         assert int(model.argmax.item()) == ds.argmax_first(logits)
     model.close()
+
+
+def test_token_step_long_context(q):
+    """Positions up to 519 of a one-layer model: the attention level's chunks of 32
+    positions spread over the fifteen consumer warps, a second round of chunks
+    from position 480, and the warps' states merged. Checked at the boundaries."""
+    cfg1 = dict(dim=256, hidden=512, n_layers=1, n_heads=4, n_kv_heads=2, vocab=300)
+    max_seq = 520
+    m = synth.gen_llama_model(seed=78, norm_scale=0.02, **cfg1)
+    t = lambda a: dev(a)
+    layers = [{**{k: (lw[k][0], t(lw[k][3])) for k in synth.LAYER_TENSORS},
+               "attn_norm": t(lw["attn_norm"]), "ffn_norm": t(lw["ffn_norm"])} for lw in m["layers"]]
+    model = q.Llama(max_seq=max_seq, embd=(m["token_embd"][0], t(m["token_embd"][3])), layers=layers,
+                    output_norm=t(m["output_norm"]), output=(m["output"][0], t(m["output"][3])), **cfg1)
+    w = ds.from_blocks(ds.LlamaConfig(max_seq=max_seq, **cfg1), m)
+    kc, vc = ds.new_cache(w.cfg)
+    check = {0, 31, 32, 33, 250, 479, 480, 481, 519}
+    for pos in range(max_seq):
+        tok = (pos * 37 + 11) % cfg1["vocab"]
+        model.forward(tok, pos)
+        if pos not in check:
+            continue
+        assert q.get_device_status() == 0
+        kg, vg = model.k_cache.cpu().numpy(), model.v_cache.cpu().numpy()
+        kc[:, :pos], vc[:, :pos] = kg[:, :pos], vg[:, :pos]
+        tr = {}
+        ref = ds.forward(w, kc, vc, tok, pos, trace=tr, rows={"k": kg[:, pos], "v": vg[:, pos]})
+        ot, orows, ocols, ob = m["output"]
+        _, S = oracle.gemv(ot, ob, orows, ocols, tr["hn"].astype(np.float32)[None, :])
+        err = np.abs(model.logits.cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= 1e-4 * S[0] + 1e-6), (pos, float(err.max()))
+    model.close()
