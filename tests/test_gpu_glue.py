@@ -292,3 +292,35 @@ def test_token_step_long_context(q):
         err = np.abs(model.logits.cpu().numpy().astype(np.float64) - ref)
         assert np.all(err <= 1e-4 * S[0] + 1e-6), (pos, float(err.max()))
     model.close()
+
+
+@pytest.mark.parametrize("batch", [3, 8])
+def test_plan_options_batched(q, batch):
+    """rmsnorm (per batch column), SwiGLU and the residual add in the 4- and
+    8-column instantiations of the streaming kernel."""
+    rng = np.random.default_rng(50 + batch)
+    dim, hid = 2048, 5632
+    Wg = synth.gen_matrix(synth.Q4_K, hid, dim, 21)
+    Wd = synth.gen_matrix(synth.Q6_K, dim, hid, 22)
+    h0 = (rng.standard_normal((batch, dim)) * rng.uniform(0.5, 3, (batch, 1))).astype(np.float32)
+    nw = rng.uniform(0.01, 0.03, dim).astype(np.float32)
+    u = rng.standard_normal((batch, hid)).astype(np.float32)
+    h = dev(h0.copy())
+    g = torch.zeros(batch, hid, device="cuda")
+    ud = dev(u)
+    plan = q.Plan([(synth.Q4_K, dev(Wg), hid, dim, h, g), (synth.Q6_K, dev(Wd), dim, hid, g, h)], [0, 1], batch,
+                  opts=[{"x_op": q.X_RMSNORM, "norm_w": dev(nw), "eps": 1e-5},
+                        {"x_op": q.X_SWIGLU, "x2": ud, "y_op": q.Y_ADD}])
+    plan.run()
+    assert q.get_device_status() == 0
+    g_gpu, h_gpu = g.cpu().numpy(), h.cpu().numpy()
+    xn = np.stack([ds.rmsnorm(h0[b], nw) for b in range(batch)]).astype(np.float32)
+    gr, gS = oracle.gemv(synth.Q4_K, Wg, hid, dim, xn)
+    for b in range(batch):
+        assert_gemv_close(g_gpu[b], gr[b], gS[b], f"rmsnorm gate, column {b}")
+    xs = np.stack([ds.swiglu(g_gpu[b], u[b]) for b in range(batch)]).astype(np.float32)
+    dr, dS = oracle.gemv(synth.Q6_K, Wd, dim, hid, xs)
+    for b in range(batch):
+        assert_gemv_close(h_gpu[b], h0[b] + dr[b], dS[b], f"swiglu down + residual, column {b}",
+                          extra=np.abs(h_gpu[b]) * 2.0 ** -23)
+    plan.close()
