@@ -106,7 +106,7 @@ struct Smem {
     static constexpr int kX = Cfg<BT>::kRingBytes;
     static constexpr int kPart = kX + Cfg<BT>::kXFloats * 4;
     static constexpr int kDst = kPart + kPartFloats * 4;               // y address of each buffer row
-    static constexpr int kDstStride = kDst + Cfg<BT>::kBufRows * 8;    // its batch-column stride (BT > 1)
+    static constexpr int kDstStride = kDst + Cfg<BT>::kBufRows * 8;    // its batch-column stride (BT > 1) or scale (BT = 1)
     static constexpr int kRanges = kDstStride + Cfg<BT>::kBufRows * 4;
     static constexpr int kRing = kRanges + 2 * MAXD * 8;              // producer: live tiles' ring ranges
     static constexpr int kBars = kRing + 2 * kSlots * 4;
@@ -446,7 +446,7 @@ QDQ_DEV float4 x_in(const DevDesc &d, const DescEx &ex, int b, int col, int off,
 
 template <int BT>
 QDQ_DEV void stage_xb(const DevDesc &d, const DescEx &ex, int kinds, int batch, int w0, int w1, int cw, int ncw,
-                      int lane, const float (&inv)[BT], float *xbuf) {
+                      int lane, const float (&inv)[BT], float *xbuf, float *sumsq = nullptr) {
     const int nk = nkinds(kinds), stride = xfloats_per_chunk<BT>(kinds);
     const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
     for (int i = cw; i < (w1 - w0) * kSlicesPerChunk; i += ncw) {
@@ -457,10 +457,13 @@ QDQ_DEV void stage_xb(const DevDesc &d, const DescEx &ex, int kinds, int batch, 
         for (int b = 0; b < BT; ++b) {
             const bool ok = b < batch && col < d.cols;
             const float *xr = d.x + (int64_t)b * d.cols + col;
-            const float4 a =
-                ok ? x_in<BT>(d, ex, b, col, 0, inv, __ldcg((const float4 *)xr)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 c =
-                ok ? x_in<BT>(d, ex, b, col, 4, inv, __ldcg((const float4 *)(xr + 4))) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 ra = ok ? __ldcg((const float4 *)xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 rc = ok ? __ldcg((const float4 *)(xr + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (sumsq != nullptr && b == 0)  // this lane's share of sum x^2 (rmsnorm folded into the flush)
+                *sumsq += ((ra.x * ra.x + ra.y * ra.y) + (ra.z * ra.z + ra.w * ra.w)) +
+                          ((rc.x * rc.x + rc.y * rc.y) + (rc.z * rc.z + rc.w * rc.w));
+            const float4 a = ok ? x_in<BT>(d, ex, b, col, 0, inv, ra) : ra;
+            const float4 c = ok ? x_in<BT>(d, ex, b, col, 4, inv, rc) : rc;
             int slot = 0;
             if (kinds & 1) {
                 float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
@@ -1027,9 +1030,9 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
-// ATTN: the plan has attention levels. Only that instantiation holds the attention
-// code: compiled into the tile callback of the others, it slowed their GEMV levels
-// by a few per cent (and by more as an out-of-line call).
+// ATTN: the plan has attention levels (the model's plan). Only that instantiation
+// holds the attention code and the rmsnorm folded into the flush: compiled into the
+// others, they slowed their GEMV levels by a few per cent.
 template <int BT, int MAXD, int MAXL, bool ATTN>
 __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __grid_constant__ StreamArgs<MAXD, MAXL> a) {
     using SM = Smem<BT, MAXD>;
@@ -1118,6 +1121,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
     const int r8 = lane >> 2, c = lane & 3;
     float *mypart = part + cw * kBufRows * BT;
     int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0;
+    float row_scale = 1.f;  // 1 / rms of the staged x when its rmsnorm is folded into the flush
     int buf_rows = 0, rg_base = 0;
     uint32_t ring_next = 0;
     bool had_tiles = false, dep_pending = false, level_staged = false;
@@ -1136,6 +1140,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
             for (int w = 0; w < kCW; ++w) sum += part[w * kBufRows + i];
             const uint64_t d = dst[i];
             float *yp = (float *)(uintptr_t)(d & ~(uint64_t)3);
+            if constexpr (ATTN) sum *= reinterpret_cast<const float *>(dstride)[i];  // 1 / rms of a folded rmsnorm, else 1
             if (d & 1) sum += __ldcg(yp);
             *yp = sum;
             if (d & 2) {
@@ -1205,9 +1210,31 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 float inv[BT];
 #pragma unroll
                 for (int b = 0; b < BT; ++b) inv[b] = 1.f;
-                if (desc_xop(d) == QDQ_X_RMSNORM) rms_scale<BT>(d, a.ex[tl.g], a.batch, cw, kCW, lane, red, inv);
-                stage_xb<BT>(d, a.ex[tl.g], tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf);
+                // rmsnorm at batch 1 with the whole vector in this window: x * w is
+                // staged, the lanes add up x^2 on the way, and 1 / rms scales each
+                // row's sum at the flush (a scalar factors out of the dot product),
+                // so x is read once and no extra barrier is needed
+                // (only in the model's instantiation: the extra per-row scale at the
+                // flush measured 1 % on the GEMV-only step)
+                const bool fold = ATTN && BT == 1 && desc_xop(d) == QDQ_X_RMSNORM && tl.xw0 == 0 &&
+                                  tl.xwn * kChunk >= d.cols;
+                if (desc_xop(d) == QDQ_X_RMSNORM && !fold)
+                    rms_scale<BT>(d, a.ex[tl.g], a.batch, cw, kCW, lane, red, inv);
+                float ss = 0.f;
+                stage_xb<BT>(d, a.ex[tl.g], tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf,
+                             fold ? &ss : nullptr);
+                if (fold) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+                    if (lane == 0) red[cw] = ss;
+                }
                 named_bar_sync(kFlushBar, kCW * 32);
+                row_scale = 1.f;
+                if (fold) {  // every thread adds the warps' sums in warp order
+                    float t = 0.f;
+                    for (int w = 0; w < kCW; ++w) t += red[w];
+                    row_scale = 1.0f / sqrtf(t / (float)d.cols + a.ex[tl.g].eps);
+                }
                 level_staged = true;
             }
             if (tl.first) {  // a new row group: its rows in the partial buffer
@@ -1216,11 +1243,16 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 rg_base = buf_rows;
                 buf_rows += tl.nrows;
                 if (cw == 0)
-                    for (int i = lane; i < tl.nrows; i += 32)
+                    for (int i = lane; i < tl.nrows; i += 32) {
                         dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) |
                                            ((tl.first_win && desc_yop(d) == QDQ_Y_STORE) ? 0u : 1u) |
-                                               (desc_amax(d) ? 2u : 0u),
-                        dstride[rg_base + i] = (int)d.rows;
+                                           (desc_amax(d) ? 2u : 0u);
+                        // batch 1: the row's scale at the flush; wider: y's column stride
+                        if constexpr (BT == 1 && ATTN)
+                            reinterpret_cast<float *>(dstride)[rg_base + i] = row_scale;
+                        else if constexpr (BT > 1)
+                            dstride[rg_base + i] = (int)d.rows;
+                    }
                 if constexpr (BT == 1) {  // batch 1 adds every unit into the warp's column
                     for (int i = lane; i < tl.nrows; i += 32) mypart[rg_base + i] = 0.f;
                     __syncwarp();
