@@ -21,18 +21,27 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t *__restrict_
                                                       float *__restrict__ out) {
     constexpr int kQuads = fmt_weights(TYPE) / 4;  // quads per block
     constexpr int kBytes = fmt_bytes(TYPE);
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < nquads; t += stride) {
-        const int64_t b = t / kQuads;
-        const int e0 = (int)(t - b * kQuads) * 4;
-        reinterpret_cast<float4 *>(out)[t] = decode4<TYPE>(blocks + b * kBytes, e0);
+    // A warp takes 64 consecutive quads: lane l decodes quads l and l + 32 (two
+    // independent decodes in flight per thread; each store instruction of the warp
+    // still writes 512 contiguous bytes).
+    const int lane = threadIdx.x & 31;
+    const int64_t nspans = (nquads + 63) / 64;
+    const int64_t wstride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nspans; w += wstride) {
+        const int64_t t0 = 64 * w + lane, t1 = t0 + 32;
+        const int64_t b0 = t0 / kQuads, b1 = t1 / kQuads;
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+        if (t0 < nquads) v0 = decode4<TYPE>(blocks + b0 * kBytes, (int)(t0 - b0 * kQuads) * 4);
+        if (t1 < nquads) v1 = decode4<TYPE>(blocks + b1 * kBytes, (int)(t1 - b1 * kQuads) * 4);
+        if (t0 < nquads) reinterpret_cast<float4 *>(out)[t0] = v0;
+        if (t1 < nquads) reinterpret_cast<float4 *>(out)[t1] = v1;
     }
 }
 
 int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStream_t stream, int sm_count) {
     const int64_t nquads = n / 4;
     const int threads = 256;
-    int64_t want = (nquads + threads - 1) / threads;
+    int64_t want = (nquads / 2 + threads - 1) / threads;  // two quads per thread
     const int64_t cap = (int64_t)sm_count * 8;
     const int grid = (int)(want < cap ? want : cap);
     if (grid <= 0) return QDQ_OK;

@@ -224,7 +224,8 @@ def llama_shapes(dim: int, hidden: int, n_heads: int, n_kv_heads: int) -> dict:
 
 
 def gen_llama_model(dim: int, hidden: int, n_layers: int, n_heads: int, n_kv_heads: int, vocab: int,
-                    seed: int, embd_type: int = Q4_K, out_type: int = Q6_K, norm_scale: float = 1.0) -> dict:
+                    seed: int, embd_type: int = Q4_K, out_type: int = Q6_K, norm_scale: float = 1.0,
+                    layer_types: dict | None = None) -> dict:
     """Raw blocks of every tensor and the fp32 norm vectors (times norm_scale), from one seed.
 
     With the workload's block draws a weight is of order 1, so q.k scores reach
@@ -238,7 +239,7 @@ def gen_llama_model(dim: int, hidden: int, n_layers: int, n_heads: int, n_kv_hea
         lw = {}
         for name in LAYER_TENSORS:
             r, c = shapes[name]
-            t = LAYER_TYPES[name]
+            t = (layer_types or LAYER_TYPES)[name]
             lw[name] = (t, r, c, gen_blocks(t, r * c // BLOCK_WEIGHTS[t], rng))
         lw["attn_norm"] = (norm_scale * rng.uniform(0.5, 1.5, dim)).astype(np.float32)
         lw["ffn_norm"] = (norm_scale * rng.uniform(0.5, 1.5, dim)).astype(np.float32)

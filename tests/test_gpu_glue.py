@@ -230,10 +230,15 @@ def _gpu_model(q, m, max_seq):
                    output=(o[0], t(o[3])), **CFG)
 
 
-@pytest.mark.parametrize("norm_scale", [0.02, 1.0])
-def test_token_step(q, norm_scale):
+PETIT_TYPES = {"q": synth.Q8_0, "k": synth.Q4_0, "v": synth.Q8_0, "o": synth.Q4_0, "gate": synth.Q8_0,
+               "up": synth.Q4_0, "down": synth.Q8_0}
+
+
+@pytest.mark.parametrize("norm_scale,petit", [(0.02, False), (1.0, False), (0.02, True)])
+def test_token_step(q, norm_scale, petit):
     max_seq = 8
-    m = synth.gen_llama_model(seed=77, norm_scale=norm_scale, **CFG)
+    kw = dict(layer_types=PETIT_TYPES, embd_type=synth.Q8_0, out_type=synth.Q4_0) if petit else {}
+    m = synth.gen_llama_model(seed=77, norm_scale=norm_scale, **kw, **CFG)
     model = _gpu_model(q, m, max_seq)
     assert model.launches == 2  # the embedding row's decode, then one plan launch
     cfg = ds.LlamaConfig(max_seq=max_seq, **CFG)
