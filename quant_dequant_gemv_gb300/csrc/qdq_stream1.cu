@@ -830,7 +830,7 @@ QDQ_DEV void tile_slices_b(const Tile &tl, const DevDesc &d, const uint8_t *stag
 // the tile's first chunk has zeroed.
 template <int TYPE, int NR>
 QDQ_DEV void tile_units1_nr(const Tile &tl, const DevDesc &d, const uint8_t *stage_p, const RowGeo &geo,
-                            const float *xbuf, int cw, int r8, int c, float *mycol, int nslices) {
+                            const float *xbuf, int first, int r8, int c, float *mycol, int nslices) {
     constexpr int QK = (TYPE == QDQ_Q4_K || TYPE == QDQ_Q6_K) ? 256 : 32;
     constexpr int SB = (kSlice / QK) * blk_bytes(TYPE);
     constexpr int KIND = x_kind(TYPE);
@@ -840,8 +840,9 @@ QDQ_DEV void tile_units1_nr(const Tile &tl, const DevDesc &d, const uint8_t *sta
     const int stride = xfloats_per_chunk<1>(tl.skinds);
     const int n = tl.nrows, rows_pp = 8 * NR;
     const int npass = (n + rows_pp - 1) / rows_pp;
-    // unit u = p * nslices + kk, stepped by kCW without divisions in the loop
-    int p = cw / nslices, kk = cw - p * nslices;
+    // unit u = p * nslices + kk from this warp's first unit, stepped by kCW
+    // without divisions in the loop
+    int p = first / nslices, kk = first - p * nslices;
     const int dp = kCW / nslices, dk = kCW - dp * nslices;
     for (; p < npass; p += dp, kk += dk) {
         if (kk >= nslices) {
@@ -859,19 +860,28 @@ QDQ_DEV void tile_units1_nr(const Tile &tl, const DevDesc &d, const uint8_t *sta
     }
 }
 
+// The units of a level are dealt to the warps round-robin across its tiles: unit
+// g of the level (counting this CTA's earlier tiles, `uoff` = their units mod kCW,
+// the same in every warp) goes to warp g mod kCW, so the remainders of successive
+// tiles fall on different warps and no warp runs more than its share plus one.
 template <int TYPE>
 QDQ_DEV void tile_units1(const Tile &tl, const DevDesc &d, const uint8_t *stage_p, const RowGeo &geo,
-                         const float *xbuf, int cw, int r8, int c, float *mycol) {
+                         const float *xbuf, int cw, int r8, int c, float *mycol, int &uoff) {
     constexpr int kCW = Cfg<1>::kCW;
     const int nslices = (tl.ccols + kSlice - 1) / kSlice;
     // rounds of units each warp runs; a unit of NR rows costs about NR + 1 row
     // units (its fixed part: pointers, scales, the row reduction)
-    const int rounds1 = (((tl.nrows + 7) / 8) * nslices + kCW - 1) / kCW;
-    const int rounds2 = (((tl.nrows + 15) / 16) * nslices + kCW - 1) / kCW;
-    if (3 * rounds2 <= 2 * rounds1)
-        tile_units1_nr<TYPE, 2>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, nslices);
-    else
-        tile_units1_nr<TYPE, 1>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, nslices);
+    const int units1 = ((tl.nrows + 7) / 8) * nslices, units2 = ((tl.nrows + 15) / 16) * nslices;
+    const int rounds1 = (units1 + kCW - 1) / kCW;
+    const int rounds2 = (units2 + kCW - 1) / kCW;
+    const int first = (cw - uoff + kCW) % kCW;  // this warp's first unit of the tile
+    if (3 * rounds2 <= 2 * rounds1) {
+        tile_units1_nr<TYPE, 2>(tl, d, stage_p, geo, xbuf, first, r8, c, mycol, nslices);
+        uoff = (uoff + units2) % kCW;
+    } else {
+        tile_units1_nr<TYPE, 1>(tl, d, stage_p, geo, xbuf, first, r8, c, mycol, nslices);
+        uoff = (uoff + units1) % kCW;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1122,6 +1132,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
     float *mypart = part + cw * kBufRows * BT;
     int t = 0, cur_e = -1, cur_level = 0, tiles_in_level = 0;
     float row_scale = 1.f;  // 1 / rms of the staged x when its rmsnorm is folded into the flush
+    int uoff = 0;           // batch 1: units of the level's earlier tiles, mod the consumer warps
     int buf_rows = 0, rg_base = 0;
     uint32_t ring_next = 0;
     bool had_tiles = false, dep_pending = false, level_staged = false;
@@ -1179,6 +1190,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
         [&](int L) {
             cur_level = L;
             tiles_in_level = 0;
+            uoff = 0;
             dep_pending = L > 0 && levels_synced;
             level_staged = false;
         },
@@ -1281,10 +1293,10 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 float *mycol = mypart + rg_base * BT;
                 if constexpr (BT == 1) {
                     switch (d.type) {
-                        case QDQ_Q4_K: tile_units1<QDQ_Q4_K>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
-                        case QDQ_Q6_K: tile_units1<QDQ_Q6_K>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
-                        case QDQ_Q8_0: tile_units1<QDQ_Q8_0>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
-                        default: tile_units1<QDQ_Q4_0>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol); break;
+                        case QDQ_Q4_K: tile_units1<QDQ_Q4_K>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, uoff); break;
+                        case QDQ_Q6_K: tile_units1<QDQ_Q6_K>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, uoff); break;
+                        case QDQ_Q8_0: tile_units1<QDQ_Q8_0>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, uoff); break;
+                        default: tile_units1<QDQ_Q4_0>(tl, d, stage_p, geo, xbuf, cw, r8, c, mycol, uoff); break;
                     }
                 } else {
                     switch (d.type) {
