@@ -892,14 +892,100 @@ QDQ_DEV void tile_units1(const Tile &tl, const DevDesc &d, const uint8_t *stage_
 //  * the pair angles pos * f_i formed and reduced by 2 pi in double (four double
 //    operations), sincosf of the reduced angle; q_h and k_g turned, k and v
 //    rounded to fp16; the group's first head stores them at row pos;
-//  * warp w scores the 32-position chunks w, w + NCW, ... (lane i: position
-//    c0 + i over the whole head) and adds the chunk's weighted values (lanes over
-//    dim pairs), keeping a running maximum, sum and value sum; the current
-//    position's key and value come from shared memory;
+//  * warp w scores the chunks w, w + NCW, ... of eight positions (heads of 32
+//    or 64 dimensions: four lanes per position, loads one chunk ahead) or of 32
+//    (other heads: lane i takes position c0 + i over the whole head) and adds
+//    the chunk's weighted values (lanes over dim pairs), keeping a running
+//    maximum, sum and value sum; the current position's key and value come from
+//    shared memory;
 //  * the warps' states merged in warp order into out[h].
 // q, k, v were written by the previous level on other SMs: read through L2.
 // ---------------------------------------------------------------------------
 constexpr int kAttnMaxD = 256;
+
+// Positions of one head in chunks of eight per warp (chunk c0 = 8 w, 8 (w + NCW),
+// ...), for heads of 32 or 64 dimensions. Lane 4 j + e holds the quarter e of
+// position c0 + j's key (one or two 16-byte loads) and value dimensions (2 lane,
+// 2 lane + 1) of the chunk's eight positions; each chunk's loads are issued one
+// chunk ahead of their use, so a warp waits for about one round trip to L2 for
+// its first chunk and little for the rest. Cache rows at or after pos are not
+// read: row pos comes from shared memory (kcur, vcur), later positions have
+// p = 0. Online softmax state (m, l, a0, a1) as in the per-32 loop.
+template <int NCW>
+QDQ_DEV void attend_chunks8(const __half *kc, const __half *vc, int kvd, int g, int D, int pos, int cw, int lane,
+                            const float *qs, const float *kcur, const float *vcur, float inv, float &m, float &l,
+                            float &a0, float &a1) {
+    const int j = lane >> 2, e4 = lane & 3, dq = D / 4;
+    const bool two = dq == 16, vin = 2 * lane < D;
+    const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+    const __half2 z2 = __float2half2_rn(0.f);
+    uint4 kn0 = z4, kn1 = z4;
+    __half2 vn[8];
+    auto load = [&](int c0) {
+        const int t = c0 + j;
+        const bool kin = t < pos;
+        const uint4 *kp = reinterpret_cast<const uint4 *>(kc + (int64_t)(kin ? t : 0) * kvd + g * D + e4 * dq);
+        kn0 = kin ? __ldcg(kp) : z4;
+        kn1 = kin && two ? __ldcg(kp + 1) : z4;
+        const __half2 *vp = reinterpret_cast<const __half2 *>(vc + (int64_t)c0 * kvd + g * D) + lane;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) vn[u] = vin && c0 + u < pos ? __ldcg(vp + (int64_t)u * (kvd / 2)) : z2;
+    };
+    int c0 = 8 * cw;
+    if (c0 <= pos) load(c0);
+    for (; c0 <= pos; c0 += 8 * NCW) {
+        const uint4 k0 = kn0, k1 = kn1;
+        __half2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = vn[u];
+        if (c0 + 8 * NCW <= pos) load(c0 + 8 * NCW);
+        const int t = c0 + j, q0 = e4 * dq;
+        float dot = 0.f;
+        if (t == pos) {
+            for (int e = q0; e < q0 + dq; ++e) dot += qs[e] * kcur[e];
+        } else {
+            const uint32_t w8[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i < 4 || two) {
+                    const float lo = __half2float(__ushort_as_half((unsigned short)(w8[i] & 0xFFFFu)));
+                    const float hi = __half2float(__ushort_as_half((unsigned short)(w8[i] >> 16)));
+                    dot += qs[q0 + 2 * i] * lo + qs[q0 + 2 * i + 1] * hi;
+                }
+            }
+        }
+        dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
+        dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 2);
+        const float s = t <= pos ? dot * inv : -INFINITY;
+        float cm = s;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+        const float mn = fmaxf(m, cm);  // finite: position c0 <= pos is in the chunk
+        const float scale = expf(m - mn);
+        const float p = t <= pos ? expf(s - mn) : 0.f;
+        float ps = e4 == 0 ? p : 0.f;  // each position once
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xFFFFFFFFu, ps, o);
+        l = l * scale + ps;
+        a0 *= scale;
+        a1 *= scale;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float pu = __shfl_sync(0xFFFFFFFFu, p, 4 * u);
+            const float2 f = __half22float2(v[u]);
+            a0 += pu * f.x;
+            a1 += pu * f.y;
+        }
+        if (pos < c0 + 8) {  // the current position's value, from shared memory
+            const float pu = __shfl_sync(0xFFFFFFFFu, p, 4 * (pos - c0));
+            if (vin) {
+                a0 += pu * vcur[2 * lane];
+                a1 += pu * vcur[2 * lane + 1];
+            }
+        }
+        m = mn;
+    }
+}
 
 template <int NCW, class A>
 QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &tl, int ctid, int cw, int lane,
@@ -909,7 +995,7 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
     float *wm = vcur + kAttnMaxD, *wl = wm + 32, *wacc = wl + 32;  // wacc[NCW][kAttnMaxD]
     const __half *kc = reinterpret_cast<const __half *>(ex.kc), *vc = reinterpret_cast<const __half *>(ex.vc);
     const float inv = 1.0f / sqrtf((float)D);
-    const bool vec = (D & 7) == 0;
+    const bool vec = (D & 7) == 0, chunks8 = D == 32 || D == 64;
     constexpr int kPer2 = kAttnMaxD / 64;
     for (int h = (int)tl.row0; h < (int)tl.row0 + tl.nrows; ++h) {
         const int g = h / kv_mul;
@@ -942,7 +1028,10 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
         float m = -INFINITY, l = 0.f, acc[2 * kPer2];
 #pragma unroll
         for (int j = 0; j < 2 * kPer2; ++j) acc[j] = 0.f;
-        for (int c0 = 32 * cw; c0 <= pos; c0 += 32 * NCW) {
+        if (chunks8)
+            attend_chunks8<NCW>(kc, vc, kvd, g, D, pos, cw, lane, qs, kcur, vcur, inv,
+                                m, l, acc[0], acc[1]);
+        for (int c0 = 32 * cw; !chunks8 && c0 <= pos; c0 += 32 * NCW) {
             const int t = c0 + lane;
             float s = -INFINITY;
             if (t <= pos) {

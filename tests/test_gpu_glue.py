@@ -267,13 +267,10 @@ def test_token_step(q, norm_scale, petit):
     model.close()
 
 
-def test_token_step_long_context(q):
-    """Positions up to 519 of a one-layer model: the attention level's chunks of 32
-    positions spread over the fifteen consumer warps, a second round of chunks
-    from position 480, and the warps' states merged. Checked at the boundaries."""
-    cfg1 = dict(dim=256, hidden=512, n_layers=1, n_heads=4, n_kv_heads=2, vocab=300)
-    max_seq = 520
-    m = synth.gen_llama_model(seed=78, norm_scale=0.02, **cfg1)
+def _check_positions(q, cfg1, max_seq, check, seed):
+    """Decode positions 0 .. max_seq - 1 of a model of shape cfg1 and compare the
+    logits with the oracle's at the positions in `check`."""
+    m = synth.gen_llama_model(seed=seed, norm_scale=0.02, **cfg1)
     t = lambda a: dev(a)
     layers = [{**{k: (lw[k][0], t(lw[k][3])) for k in synth.LAYER_TENSORS},
                "attn_norm": t(lw["attn_norm"]), "ffn_norm": t(lw["ffn_norm"])} for lw in m["layers"]]
@@ -281,7 +278,6 @@ def test_token_step_long_context(q):
                     output_norm=t(m["output_norm"]), output=(m["output"][0], t(m["output"][3])), **cfg1)
     w = ds.from_blocks(ds.LlamaConfig(max_seq=max_seq, **cfg1), m)
     kc, vc = ds.new_cache(w.cfg)
-    check = {0, 31, 32, 33, 250, 479, 480, 481, 519}
     for pos in range(max_seq):
         tok = (pos * 37 + 11) % cfg1["vocab"]
         model.forward(tok, pos)
@@ -297,6 +293,24 @@ def test_token_step_long_context(q):
         err = np.abs(model.logits.cpu().numpy().astype(np.float64) - ref)
         assert np.all(err <= 1e-4 * S[0] + 1e-6), (pos, float(err.max()))
     model.close()
+
+
+def test_token_step_long_context(q):
+    """Positions up to 519 of a one-layer model with 64-dimensional heads: the
+    attention level's chunks of eight positions spread over the fifteen consumer
+    warps (a new round every 120 positions, each warp's next chunk loaded ahead),
+    and the warps' states merged. Checked at the chunk and round boundaries."""
+    cfg1 = dict(dim=256, hidden=512, n_layers=1, n_heads=4, n_kv_heads=2, vocab=300)
+    _check_positions(q, cfg1, 520, {0, 7, 8, 9, 31, 32, 33, 119, 120, 121, 239, 240, 250, 479, 480, 481, 519}, 78)
+
+
+@pytest.mark.parametrize("n_heads,n_kv_heads", [(8, 2), (2, 1), (8, 8)])
+def test_token_step_head_dims(q, n_heads, n_kv_heads):
+    """Heads of 32 dimensions (the eight-position chunks with one 16-byte key load
+    per lane) and of 128 (the per-32-position loop), grouped and ungrouped, over
+    several rounds of chunks."""
+    cfg1 = dict(dim=256, hidden=512, n_layers=1, n_heads=n_heads, n_kv_heads=n_kv_heads, vocab=300)
+    _check_positions(q, cfg1, 136, {0, 7, 8, 31, 32, 64, 119, 120, 135}, 79 + n_heads)
 
 
 @pytest.mark.parametrize("batch", [3, 8])
