@@ -173,9 +173,16 @@ int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int bat
  *         QDQ_X_SWIGLU   it reads silu(x) * x2 with silu(g) = g / (1 + exp(-g));
  *                        x is the gate output, x2 the up output, both
  *                        [batch][cols].
+ *         QDQ_X_MUL      it reads x * x2 elementwise (x2 [cols]; batch 1): with
+ *                        a gate GEMV stored through QDQ_Y_SILU, the same SwiGLU
+ *                        product with silu evaluated once per element instead
+ *                        of once per CTA that stages it.
  *   y_op  QDQ_Y_STORE    y = W x' (as qdq_gemv).
  *         QDQ_Y_ADD      y += W x' (a residual addition; y must not be read by
  *                        another GEMV of the same level).
+ *         QDQ_Y_SILU     y = silu(W x'), the same silu as QDQ_X_SWIGLU's. Batch
+ *                        1 and cols <= 4096 (a row's sum is complete in one
+ *                        store).
  *   argmax  NULL, or a device int64: after the run it holds the index of the
  *           largest y of this GEMV (the smallest such index on ties). At most
  *           one GEMV of a plan, in its last level, batch 1, cols <= 8192.
@@ -185,8 +192,8 @@ int qdq_plan_create(const qdq_gemv_desc *descs, const int *level, int n, int bat
  * QDQ_ERR_ALIGN for a bad x2, norm_w or argmax pointer. The plan then also
  * owns 16 bytes of device memory for the argmax.
  * ------------------------------------------------------------------------- */
-enum qdq_x_op { QDQ_X_PLAIN = 0, QDQ_X_RMSNORM = 1, QDQ_X_SWIGLU = 2 };
-enum qdq_y_op { QDQ_Y_STORE = 0, QDQ_Y_ADD = 1 };
+enum qdq_x_op { QDQ_X_PLAIN = 0, QDQ_X_RMSNORM = 1, QDQ_X_SWIGLU = 2, QDQ_X_MUL = 3 };
+enum qdq_y_op { QDQ_Y_STORE = 0, QDQ_Y_ADD = 1, QDQ_Y_SILU = 2 };
 typedef struct qdq_gemv_opts {
     int32_t x_op;
     int32_t y_op;
@@ -265,11 +272,13 @@ int qdq_rope_attention(const float *q, const float *k, const float *v, uint16_t 
  * dim x dim; k, v: kv x dim (kv = n_kv_heads * dim / n_heads); gate, up:
  * hidden x dim; down: dim x hidden. Norm weights are fp32 device vectors [dim].
  * The model allocates its activations, the fp16 key/value cache
- * ([n_layers][max_seq][kv] each) and its plans in create, and frees them in
- * destroy. A forward call runs 2 + 2 n_layers launches on `stream`: the
- * embedding row's decode, the first layer's q/k/v, then per layer the attention
- * launch and one plan (o, gate/up, down, next q/k/v or the head). Positions
- * must be run in order 0, 1, ... (a position reads the cache rows before it).
+ * ([n_layers][max_seq][kv] each) and one plan in create, and frees them in
+ * destroy. A forward call runs 2 launches on `stream`: the embedding row's
+ * decode, then one plan of every layer's levels (q/k/v with the attention norm;
+ * attention; o with the residual; gate/up with the FFN norm, the gate stored
+ * through silu when dim <= 4096; down reading gate * up, or silu(gate) * up
+ * when wider, with the residual) and the head with its argmax. Positions must
+ * be run in order 0, 1, ... (a position reads the cache rows before it).
  * qdq_llama_buffers returns the device addresses of the logits [vocab], argmax
  * (one int64), the residual stream h [dim] and the two caches.
  * ------------------------------------------------------------------------- */

@@ -223,13 +223,18 @@ static int check_opts(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
     int rc = QDQ_OK;
     for (int i = 0; i < n && !rc; ++i) {
         const qdq_gemv_opts &o = opts[i];
-        if (o.x_op < QDQ_X_PLAIN || o.x_op > QDQ_X_SWIGLU || o.y_op < QDQ_Y_STORE || o.y_op > QDQ_Y_ADD)
+        if (o.x_op < QDQ_X_PLAIN || o.x_op > QDQ_X_MUL || o.y_op < QDQ_Y_STORE || o.y_op > QDQ_Y_SILU)
             return QDQ_ERR_SHAPE;
+        // silu at the store needs each row's whole sum in one flush: batch 1 and
+        // whole-row tiles in one x window (two 2048-column chunks at least); both
+        // options run in the batch-1 kernel that also holds attention levels
+        if (o.y_op == QDQ_Y_SILU && (batch != 1 || descs[i].cols > 4096)) return QDQ_ERR_SHAPE;
+        if (o.x_op == QDQ_X_MUL && batch != 1) return QDQ_ERR_SHAPE;
         if (o.x_op == QDQ_X_RMSNORM) {
             if (!(o.eps >= 0.0f) || o.eps > 1.0f) return QDQ_ERR_SHAPE;
             rc = check_dev_ptr(o.norm_w, device);
         }
-        if (!rc && o.x_op == QDQ_X_SWIGLU) rc = check_dev_ptr(o.x2, device);
+        if (!rc && (o.x_op == QDQ_X_SWIGLU || o.x_op == QDQ_X_MUL)) rc = check_dev_ptr(o.x2, device);
         if (!rc && o.argmax) {
             if (*has_argmax || batch != 1 || level[i] != level[n - 1] || descs[i].cols > 8192) return QDQ_ERR_SHAPE;
             if (descs[i].rows > 0xFFFFFFFFll) return QDQ_ERR_SHAPE;
@@ -239,7 +244,7 @@ static int check_opts(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
         // GEMVs of one level reading the same x stage it once: same x option
         for (int k = 0; k < i && !rc; ++k)
             if (level[k] == level[i] && descs[k].x == descs[i].x &&
-                (opts[k].x_op != o.x_op || (o.x_op == QDQ_X_SWIGLU && opts[k].x2 != o.x2) ||
+                (opts[k].x_op != o.x_op || ((o.x_op == QDQ_X_SWIGLU || o.x_op == QDQ_X_MUL) && opts[k].x2 != o.x2) ||
                  (o.x_op == QDQ_X_RMSNORM && (opts[k].norm_w != o.norm_w || opts[k].eps != o.eps))))
                 return QDQ_ERR_SHAPE;
     }

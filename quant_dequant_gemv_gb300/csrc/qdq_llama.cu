@@ -357,15 +357,18 @@ int qdq_llama_create(const qdq_llama_config *cfg, const void *token_embd, int em
         D.push_back(desc(w.type[3], w.w[3], dim, dim, m->att, m->h));
         O.push_back(opt(QDQ_X_PLAIN, QDQ_Y_ADD, nullptr, nullptr, 0.f, nullptr));
         Lv.push_back(level++);
+        // (up to 4096 columns silu is applied once, as the gate is stored, and the
+        // down projection stages the product; wider, it stages silu(gate) * up)
+        const bool silu_at_store = dim <= 4096;
         D.push_back(desc(w.type[4], w.w[4], hid, dim, m->h, m->gate));
         D.push_back(desc(w.type[5], w.w[5], hid, dim, m->h, m->up));
-        for (int i = 0; i < 2; ++i) {
-            O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, w.ffn_norm, eps, nullptr));
-            Lv.push_back(level);
-        }
+        O.push_back(opt(QDQ_X_RMSNORM, silu_at_store ? QDQ_Y_SILU : QDQ_Y_STORE, nullptr, w.ffn_norm, eps, nullptr));
+        O.push_back(opt(QDQ_X_RMSNORM, QDQ_Y_STORE, nullptr, w.ffn_norm, eps, nullptr));
+        Lv.push_back(level);
+        Lv.push_back(level);
         ++level;
         D.push_back(desc(w.type[6], w.w[6], dim, hid, m->gate, m->h));
-        O.push_back(opt(QDQ_X_SWIGLU, QDQ_Y_ADD, m->up, nullptr, 0.f, nullptr));
+        O.push_back(opt(silu_at_store ? QDQ_X_MUL : QDQ_X_SWIGLU, QDQ_Y_ADD, m->up, nullptr, 0.f, nullptr));
         Lv.push_back(level++);
     }
     // logits = Wout rmsnorm(h, output_norm), with their argmax

@@ -116,10 +116,14 @@ int stream_plan_build(const qdq_gemv_desc *descs, const qdq_gemv_opts *opts, con
     p->bt = bt_of(batch);
     p->grid = sm_count;
     const int nlev = level ? level[n - 1] + 1 : 1;
-    p->big = n > kMaxGroupDescs || nlev > 1;
-    p->cooperative = nlev > 1;
     p->attn = false;
-    for (int i = 0; i < n; ++i) p->attn = p->attn || descs[i].type == kTypeAttn;
+    // the model's instantiation (plan-sized arguments): attention levels, silu
+    // applied at the store, or x * x2 staged
+    for (int i = 0; i < n; ++i)
+        p->attn = p->attn || descs[i].type == kTypeAttn ||
+                  (opts != nullptr && (opts[i].y_op == QDQ_Y_SILU || opts[i].x_op == QDQ_X_MUL));
+    p->big = n > kMaxGroupDescs || nlev > 1 || p->attn;
+    p->cooperative = nlev > 1;
     if (p->big) {
         using A = StreamArgs<kMaxPlanDescs, kMaxPlanLevels>;
         A *args = (A *)malloc(sizeof(A));

@@ -427,6 +427,48 @@ QDQ_DEV void rms_scale(const DevDesc &d, const DescEx &ex, int batch, int cw, in
 
 QDQ_DEV float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// The raw values behind x[b][col..col+7]: x itself and the operand of its option
+// (the rmsnorm weight or, for SwiGLU, the up projection; x holds the gate), all
+// four loads issued together (one round trip to L2 for the slice, not one per
+// operand).
+struct XRaw {
+    float4 a, c, pa, pc;
+};
+
+QDQ_DEV XRaw x_load(const DevDesc &d, const DescEx &ex, int b, int col, bool ok) {
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    XRaw r{z, z, z, z};
+    if (!ok) return r;
+    const float *xr = d.x + (int64_t)b * d.cols + col;
+    const int xop = desc_xop(d);
+    if (xop == QDQ_X_SWIGLU || xop == QDQ_X_MUL) {
+        const float *ur = ex.x2 + (int64_t)b * d.cols + col;
+        r.a = __ldcg((const float4 *)xr);
+        r.c = __ldcg((const float4 *)(xr + 4));
+        r.pa = __ldcg((const float4 *)ur);
+        r.pc = __ldcg((const float4 *)(ur + 4));
+    } else if (xop == QDQ_X_RMSNORM) {
+        r.a = __ldcg((const float4 *)xr);
+        r.c = __ldcg((const float4 *)(xr + 4));
+        r.pa = __ldg((const float4 *)(ex.nw + col));
+        r.pc = __ldg((const float4 *)(ex.nw + col + 4));
+    } else {
+        r.a = __ldcg((const float4 *)xr);
+        r.c = __ldcg((const float4 *)(xr + 4));
+    }
+    return r;
+}
+
+// The value the dot product reads (QDQ_X_*): as stored, rmsnorm-scaled by s,
+// silu(gate) * up, or x * x2.
+QDQ_DEV float4 x_apply(int xop, float s, float4 v, float4 p) {
+    if (xop == QDQ_X_RMSNORM) return make_float4(v.x * s * p.x, v.y * s * p.y, v.z * s * p.z, v.w * s * p.w);
+    if (xop == QDQ_X_SWIGLU)
+        return make_float4(silu(v.x) * p.x, silu(v.y) * p.y, silu(v.z) * p.z, silu(v.w) * p.w);
+    if (xop == QDQ_X_MUL) return make_float4(v.x * p.x, v.y * p.y, v.z * p.z, v.w * p.w);
+    return v;
+}
+
 // The value the dot product reads at x[b][col..col+3] (QDQ_X_*): as stored,
 // rmsnorm-scaled, or silu(gate) * up.
 template <int BT>
@@ -444,11 +486,16 @@ QDQ_DEV float4 x_in(const DevDesc &d, const DescEx &ex, int b, int col, int off,
     return v;
 }
 
-template <int BT>
+// FUSED_LOADS (the model's instantiation): x and its option operand loaded
+// together (x_load), QDQ_X_MUL included; otherwise (no QDQ_X_MUL there) the
+// operand is loaded where it is applied, which keeps the GEMV-only
+// instantiations within their registers.
+template <int BT, bool FUSED_LOADS = false>
 QDQ_DEV void stage_xb(const DevDesc &d, const DescEx &ex, int kinds, int batch, int w0, int w1, int cw, int ncw,
                       int lane, const float (&inv)[BT], float *xbuf, float *sumsq = nullptr) {
-    const int nk = nkinds(kinds), stride = xfloats_per_chunk<BT>(kinds);
+    const int stride = xfloats_per_chunk<BT>(kinds);
     const int u0 = xunit(2 * lane), u1 = xunit(2 * lane + 1);
+    const int xop = desc_xop(d);
     for (int i = cw; i < (w1 - w0) * kSlicesPerChunk; i += ncw) {
         const int j = i / kSlicesPerChunk, w = i % kSlicesPerChunk;
         float *chunk = xbuf + j * stride;
@@ -456,14 +503,23 @@ QDQ_DEV void stage_xb(const DevDesc &d, const DescEx &ex, int kinds, int batch, 
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
             const bool ok = b < batch && col < d.cols;
-            const float *xr = d.x + (int64_t)b * d.cols + col;
-            const float4 ra = ok ? __ldcg((const float4 *)xr) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 rc = ok ? __ldcg((const float4 *)(xr + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 ra, rc, a, c;
+            if constexpr (FUSED_LOADS) {
+                const XRaw r = x_load(d, ex, b, col, ok);
+                ra = r.a;
+                rc = r.c;
+                a = ok ? x_apply(xop, inv[b], ra, r.pa) : ra;
+                c = ok ? x_apply(xop, inv[b], rc, r.pc) : rc;
+            } else {
+                const float *xr = d.x + (int64_t)b * d.cols + col;
+                ra = ok ? __ldcg((const float4 *)xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+                rc = ok ? __ldcg((const float4 *)(xr + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                a = ok ? x_in<BT>(d, ex, b, col, 0, inv, ra) : ra;
+                c = ok ? x_in<BT>(d, ex, b, col, 4, inv, rc) : rc;
+            }
             if (sumsq != nullptr && b == 0)  // this lane's share of sum x^2 (rmsnorm folded into the flush)
                 *sumsq += ((ra.x * ra.x + ra.y * ra.y) + (ra.z * ra.z + ra.w * ra.w)) +
                           ((rc.x * rc.x + rc.y * rc.y) + (rc.z * rc.z + rc.w * rc.w));
-            const float4 a = ok ? x_in<BT>(d, ex, b, col, 0, inv, ra) : ra;
-            const float4 c = ok ? x_in<BT>(d, ex, b, col, 4, inv, rc) : rc;
             int slot = 0;
             if (kinds & 1) {
                 float4 *sl = (float4 *)(chunk + (slot * BT + b) * kChunk + w * kSlice);
@@ -1240,7 +1296,11 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
             for (int w = 0; w < kCW; ++w) sum += part[w * kBufRows + i];
             const uint64_t d = dst[i];
             float *yp = (float *)(uintptr_t)(d & ~(uint64_t)3);
-            if constexpr (ATTN) sum *= reinterpret_cast<const float *>(dstride)[i];  // 1 / rms of a folded rmsnorm, else 1
+            if constexpr (ATTN) {  // 1 / rms of a folded rmsnorm, else 1; its sign: silu
+                const float sc = reinterpret_cast<const float *>(dstride)[i];
+                sum *= fabsf(sc);
+                if (__float_as_uint(sc) >> 31) sum = silu(sum);
+            }
             if (d & 1) sum += __ldcg(yp);
             *yp = sum;
             if (d & 2) {
@@ -1322,7 +1382,7 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 if (desc_xop(d) == QDQ_X_RMSNORM && !fold)
                     rms_scale<BT>(d, a.ex[tl.g], a.batch, cw, kCW, lane, red, inv);
                 float ss = 0.f;
-                stage_xb<BT>(d, a.ex[tl.g], tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf,
+                stage_xb<BT, ATTN>(d, a.ex[tl.g], tl.skinds, a.batch, tl.xw0, tl.xw0 + tl.xwn, cw, kCW, lane, inv, xbuf,
                              fold ? &ss : nullptr);
                 if (fold) {
 #pragma unroll
@@ -1346,11 +1406,13 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 if (cw == 0)
                     for (int i = lane; i < tl.nrows; i += 32) {
                         dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) |
-                                           ((tl.first_win && desc_yop(d) == QDQ_Y_STORE) ? 0u : 1u) |
+                                           ((tl.first_win && desc_yop(d) != QDQ_Y_ADD) ? 0u : 1u) |
                                            (desc_amax(d) ? 2u : 0u);
-                        // batch 1: the row's scale at the flush; wider: y's column stride
+                        // batch 1: the row's scale at the flush, its sign bit set for a
+                        // row stored through silu; wider: y's column stride
                         if constexpr (BT == 1 && ATTN)
-                            reinterpret_cast<float *>(dstride)[rg_base + i] = row_scale;
+                            reinterpret_cast<float *>(dstride)[rg_base + i] =
+                                desc_yop(d) == QDQ_Y_SILU ? -row_scale : row_scale;
                         else if constexpr (BT > 1)
                             dstride[rg_base + i] = (int)d.rows;
                     }

@@ -33,8 +33,8 @@ class GemvDesc(ctypes.Structure):
 
 
 # qdq_gemv_opts: step glue fused into a plan's GEMV
-X_PLAIN, X_RMSNORM, X_SWIGLU = 0, 1, 2
-Y_STORE, Y_ADD = 0, 1
+X_PLAIN, X_RMSNORM, X_SWIGLU, X_MUL = 0, 1, 2, 3
+Y_STORE, Y_ADD, Y_SILU = 0, 1, 2
 
 
 class GemvOpts(ctypes.Structure):

@@ -1,7 +1,7 @@
 """The decode-step glue on the GPU against the oracle (oracle/decode_step.py).
 
-* Plan options: a GEMV reading rmsnorm(x) or silu(gate) * up, writing y += W x,
-  and the output head's fused argmax. The GEMV bound is the one every GEMV test
+* Plan options: a GEMV reading rmsnorm(x), silu(gate) * up or gate * up, writing
+  y += W x or silu(W x), and the output head's fused argmax. The GEMV bound is the one every GEMV test
   uses, |y - y_ref| <= 1e-5 sum|w x'| + 1e-7, with x' the oracle's input in
   double precision (the prologue's own fp32 rounding is far inside it).
 * qdq_rope_attention: the cache row it writes equals fp16 of the oracle's turned
@@ -84,6 +84,42 @@ def test_plan_swiglu_prologue_and_residual_add(q):
     # y = h0 + W x': the one extra fp32 addition rounds at |y| 2^-24
     got = y.cpu().numpy()[0]
     assert_gemv_close(got, y_ref[0] + h0, S[0], "swiglu + residual", extra=np.abs(got) * 2.0 ** -23)
+    plan.close()
+
+
+def test_plan_silu_store_then_product_stage(q):
+    """gate stored through silu (Y_SILU) and up from rmsnorm(h); down reads
+    gate * up (X_MUL) and adds into h: SwiGLU split between the two levels."""
+    rng = np.random.default_rng(41)
+    dim, hid = 2048, 5632
+    Wg, Wu, Wd = (synth.gen_matrix(t, r, c, s) for t, r, c, s in
+                  [(synth.Q4_K, hid, dim, 5), (synth.Q4_K, hid, dim, 6), (synth.Q6_K, dim, hid, 7)])
+    h0 = rng.standard_normal(dim).astype(np.float32)
+    nw = rng.uniform(0.5, 1.5, dim).astype(np.float32)
+    h = dev(h0[None, :].copy())
+    gbuf = torch.zeros(1, hid, device="cuda")
+    ubuf = torch.zeros(1, hid, device="cuda")
+    nwd = dev(nw)
+    items = [(synth.Q4_K, dev(Wg), hid, dim, h, gbuf), (synth.Q4_K, dev(Wu), hid, dim, h, ubuf),
+             (synth.Q6_K, dev(Wd), dim, hid, gbuf, h)]
+    opts = [{"x_op": q.X_RMSNORM, "norm_w": nwd, "eps": 1e-5, "y_op": q.Y_SILU},
+            {"x_op": q.X_RMSNORM, "norm_w": nwd, "eps": 1e-5},
+            {"x_op": q.X_MUL, "x2": ubuf, "y_op": q.Y_ADD}]
+    plan = q.Plan(items, [0, 0, 1], 1, opts=opts)
+    plan.run()
+    assert q.get_device_status() == 0
+    g_gpu, u_gpu, h_gpu = gbuf.cpu().numpy()[0], ubuf.cpu().numpy()[0], h.cpu().numpy()[0]
+    xn = ds.rmsnorm(h0, nw, 1e-5).astype(np.float32)[None, :]
+    gr, gS = oracle.gemv(synth.Q4_K, Wg, hid, dim, xn)
+    ur, uS = oracle.gemv(synth.Q4_K, Wu, hid, dim, xn)
+    # silu has slope below 1.1: the GEMV bound carries over, plus the fp32 rounding
+    # of silu itself (exp and the division, a few units of 2^-24)
+    assert_gemv_close(g_gpu, ds.silu(gr[0]), 1.1 * gS[0], "silu(gate)", extra=np.abs(g_gpu) * 2.0 ** -20)
+    assert_gemv_close(u_gpu, ur[0], uS[0], "up")
+    # down reads the GPU's gate * up, each product rounded once to fp32
+    xm = (g_gpu.astype(np.float64) * u_gpu).astype(np.float32)[None, :]
+    dr, dS = oracle.gemv(synth.Q6_K, Wd, dim, hid, xm)
+    assert_gemv_close(h_gpu, h0 + dr[0], dS[0], "down + residual", extra=np.abs(h_gpu) * 2.0 ** -23)
     plan.close()
 
 
@@ -172,6 +208,8 @@ def test_plan_option_checks(q):
         [{"x_op": q.X_RMSNORM, "norm_w": None}],
         [{"x_op": q.X_SWIGLU}],
         [{"argmax": am}, {"argmax": am}],  # two argmax GEMVs
+        [{"y_op": 3}],
+        [{"x_op": q.X_MUL, "x2": None}],
     ]
     for opts in bad:
         items = [(synth.Q4_K, W, 8, 256, x, y)] * len(opts)
@@ -181,6 +219,16 @@ def test_plan_option_checks(q):
     with pytest.raises(q.QdqError):
         q.Plan([(synth.Q4_K, W, 8, 256, x, y), (synth.Q4_K, W, 8, 256, x, y)], [0, 1], 1,
                opts=[{"argmax": am}, {}])
+    # silu at the store and the staged product: batch 1 only; silu rows of at most 4096 columns
+    W2 = dev(synth.gen_matrix(synth.Q4_K, 8, 4352, 2))
+    xb = torch.zeros(2, 256, device="cuda")
+    yb = torch.zeros(2, 8, device="cuda")
+    xw = torch.zeros(1, 4352, device="cuda")
+    for items, batch, opts in [([(synth.Q4_K, W, 8, 256, xb, yb)], 2, [{"y_op": q.Y_SILU}]),
+                               ([(synth.Q4_K, W, 8, 256, xb, yb)], 2, [{"x_op": q.X_MUL, "x2": xb}]),
+                               ([(synth.Q4_K, W2, 8, 4352, xw, y)], 1, [{"y_op": q.Y_SILU}])]:
+        with pytest.raises(q.QdqError):
+            q.Plan(items, [0], batch, opts=opts)
     # two GEMVs of a level read the same x with different options
     with pytest.raises(q.QdqError):
         q.Plan([(synth.Q4_K, W, 8, 256, x, y), (synth.Q4_K, W, 8, 256, x, torch.zeros(1, 8, device="cuda"))],
