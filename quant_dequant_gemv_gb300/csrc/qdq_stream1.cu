@@ -961,16 +961,38 @@ constexpr int kAttnMaxD = 256;
 
 // Positions of one head in chunks of eight per warp (chunk c0 = 8 w, 8 (w + NCW),
 // ...), for heads of 32 or 64 dimensions. Lane 4 j + e holds the quarter e of
-// position c0 + j's key (one or two 16-byte loads) and value dimensions (2 lane,
-// 2 lane + 1) of the chunk's eight positions; each chunk's loads are issued one
-// chunk ahead of their use, so a warp waits for about one round trip to L2 for
-// its first chunk and little for the rest. Cache rows at or after pos are not
-// read: row pos comes from shared memory (kcur, vcur), later positions have
-// p = 0. Online softmax state (m, l, a0, a1) as in the per-32 loop.
+// position c0 + j's key (one or two 16-byte pieces) and value dimensions (2 lane,
+// 2 lane + 1) of the chunk's eight positions. The first chunk was copied to this
+// warp's shared-memory area by kv_first_copy before the RoPE phase; every later
+// chunk is loaded into registers one chunk ahead of its use. Cache rows at or
+// after pos are not read: row pos comes from shared memory (kcur, vcur), later
+// positions have p = 0 (their copied rows are zero-filled). Online softmax state
+// (m, l, a0, a1) as in the per-32 loop.
+constexpr int kKVRowBytes = 128;                 // a copied key or value row (64 fp16)
+constexpr int kKVAreaBytes = 16 * kKVRowBytes;  // eight key rows, then eight value rows
+
+QDQ_DEV void kv_first_copy(const __half *kc, const __half *vc, int kvd, int g, int D, int pos, int c0, int lane,
+                           uint32_t area) {
+    // 64 pieces of 16 bytes per matrix: piece p = row p / 8, bytes 16 (p % 8)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int p = lane + 32 * h, row = p >> 3, off = 16 * (p & 7);
+        const bool in = c0 + row < pos && off < 2 * D;
+        const int64_t e = (int64_t)(in ? c0 + row : 0) * kvd + g * D + off / 2;  // in halves
+        const uint32_t n = in ? 16u : 0u;  // zero-fill rows at or after pos
+        const uint32_t dk = area + (uint32_t)(row * kKVRowBytes + off);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dk), "l"(kc + e), "r"(n) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dk + 8 * kKVRowBytes), "l"(vc + e),
+                     "r"(n)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
 template <int NCW>
 QDQ_DEV void attend_chunks8(const __half *kc, const __half *vc, int kvd, int g, int D, int pos, int cw, int lane,
-                            const float *qs, const float *kcur, const float *vcur, float inv, float &m, float &l,
-                            float &a0, float &a1) {
+                            const float *qs, const float *kcur, const float *vcur, float inv, const uint8_t *area,
+                            float &m, float &l, float &a0, float &a1) {
     const int j = lane >> 2, e4 = lane & 3, dq = D / 4;
     const bool two = dq == 16, vin = 2 * lane < D;
     const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
@@ -988,7 +1010,16 @@ QDQ_DEV void attend_chunks8(const __half *kc, const __half *vc, int kvd, int g, 
         for (int u = 0; u < 8; ++u) vn[u] = vin && c0 + u < pos ? __ldcg(vp + (int64_t)u * (kvd / 2)) : z2;
     };
     int c0 = 8 * cw;
-    if (c0 <= pos) load(c0);
+    if (c0 <= pos) {  // the first chunk, copied by kv_first_copy
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncwarp();
+        const uint4 *kp = reinterpret_cast<const uint4 *>(area + j * kKVRowBytes + e4 * dq * 2);
+        kn0 = kp[0];
+        kn1 = two ? kp[1] : z4;
+        const __half2 *vp = reinterpret_cast<const __half2 *>(area + 8 * kKVRowBytes) + lane;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) vn[u] = vin ? vp[u * (kKVRowBytes / 4)] : z2;
+    }
     for (; c0 <= pos; c0 += 8 * NCW) {
         const uint4 k0 = kn0, k1 = kn1;
         __half2 v[8];
@@ -1048,14 +1079,21 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
                     float *scratch) {
     const int D = d.cols, kvd = d.nkv * D, kv_mul = (int)d.rows / d.nkv, pos = a.attn_pos;
     float *qs = scratch, *kcur = qs + kAttnMaxD, *vcur = kcur + kAttnMaxD;
-    float *wm = vcur + kAttnMaxD, *wl = wm + 32, *wacc = wl + 32;  // wacc[NCW][kAttnMaxD]
+    float *wm = vcur + kAttnMaxD, *wl = wm + 32, *wacc = wl + 32;  // wacc[NCW][wst]
     const __half *kc = reinterpret_cast<const __half *>(ex.kc), *vc = reinterpret_cast<const __half *>(ex.vc);
     const float inv = 1.0f / sqrtf((float)D);
     const bool vec = (D & 7) == 0, chunks8 = D == 32 || D == 64;
+    const int wst = chunks8 ? 64 : kAttnMaxD;
+    // chunks of eight: each warp's first chunk is copied here (after wacc)
+    uint8_t *kv_area = reinterpret_cast<uint8_t *>(wacc + NCW * 64) + cw * kKVAreaBytes;
     constexpr int kPer2 = kAttnMaxD / 64;
     for (int h = (int)tl.row0; h < (int)tl.row0 + tl.nrows; ++h) {
         const int g = h / kv_mul;
         const bool writer = h % kv_mul == 0;
+        // the first chunk's cache rows (written by earlier launches) are in
+        // flight during the RoPE phase
+        if (chunks8 && 8 * cw <= pos)
+            kv_first_copy(kc, vc, kvd, g, D, pos, 8 * cw, lane, (uint32_t)__cvta_generic_to_shared(kv_area));
         for (int i = ctid; i < D / 2; i += NCW * 32) {
             const double th = (double)pos * a.rope_f[i];
             const double turns = rint(th * 0.15915494309189535);
@@ -1085,7 +1123,7 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
 #pragma unroll
         for (int j = 0; j < 2 * kPer2; ++j) acc[j] = 0.f;
         if (chunks8)
-            attend_chunks8<NCW>(kc, vc, kvd, g, D, pos, cw, lane, qs, kcur, vcur, inv,
+            attend_chunks8<NCW>(kc, vc, kvd, g, D, pos, cw, lane, qs, kcur, vcur, inv, kv_area,
                                 m, l, acc[0], acc[1]);
         for (int c0 = 32 * cw; !chunks8 && c0 <= pos; c0 += 32 * NCW) {
             const int t = c0 + lane;
@@ -1161,19 +1199,20 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
         for (int j = 0; j < kPer2; ++j) {
             const int d2 = lane + 32 * j;
             if (2 * d2 < D) {
-                wacc[cw * kAttnMaxD + 2 * d2] = acc[2 * j];
-                wacc[cw * kAttnMaxD + 2 * d2 + 1] = acc[2 * j + 1];
+                wacc[cw * wst + 2 * d2] = acc[2 * j];
+                wacc[cw * wst + 2 * d2 + 1] = acc[2 * j + 1];
             }
         }
         named_bar_sync(kFlushBar, NCW * 32);
-        float M = -INFINITY, L = 0.f;
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, wm[w]);
-        for (int w = 0; w < NCW; ++w)
-            if (wl[w] > 0.f) L += wl[w] * expf(wm[w] - M);
-        for (int e = ctid; e < D; e += NCW * 32) {
-            float o = 0.f;
+        for (int e = ctid; e < D; e += NCW * 32) {  // each warp's factor taken once per output
+            float M = -INFINITY, L = 0.f, o = 0.f;
+            for (int w = 0; w < NCW; ++w) M = fmaxf(M, wm[w]);
             for (int w = 0; w < NCW; ++w)
-                if (wl[w] > 0.f) o += wacc[w * kAttnMaxD + e] * expf(wm[w] - M);
+                if (wl[w] > 0.f) {
+                    const float f = expf(wm[w] - M);
+                    L += wl[w] * f;
+                    o += wacc[w * wst + e] * f;
+                }
             d.y[h * D + e] = o / L;
         }
         // the scratch is reused by the next head, and these stores precede the
@@ -1359,6 +1398,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
             if constexpr (ATTN) {
                 if (tl.attn) {
                     static_assert(3 * kAttnMaxD + 64 + kCW * kAttnMaxD <= Cfg<BT>::kXFloats, "attention scratch");
+                    static_assert((3 * kAttnMaxD + 64 + kCW * 64) * 4 + kCW * kKVAreaBytes <= Cfg<BT>::kXFloats * 4 &&
+                                      (3 * kAttnMaxD + 64 + kCW * 64) * 4 % 16 == 0,
+                                  "attention scratch with the first chunks' copies");
                     attend<kCW>(a, d, a.ex[tl.g], tl, ctid, cw, lane, xbuf);
                     return;
                 }
