@@ -25,9 +25,11 @@ SRC = HERE / "qdq_oracle.c"
 BUILD_DIR = HERE / "_build"
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
 
-Q4_0, Q8_0, Q4_K, Q6_K, Q5_0, Q5_1, Q8_0G, Q2_K = 1, 2, 3, 4, 5, 6, 7, 8
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210, Q5_0: 22, Q5_1: 24, Q8_0G: 34, Q2_K: 84}
-BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_0: 32, Q5_1: 32, Q8_0G: 32, Q2_K: 256}
+Q4_0, Q8_0, Q4_K, Q6_K, Q5_0, Q5_1, Q8_0G, Q2_K, Q5_K, Q3_K = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210, Q5_0: 22, Q5_1: 24, Q8_0G: 34, Q2_K: 84, Q5_K: 176,
+               Q3_K: 110}
+BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_0: 32, Q5_1: 32, Q8_0G: 32, Q2_K: 256, Q5_K: 256,
+                 Q3_K: 256}
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64

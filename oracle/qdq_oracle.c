@@ -38,7 +38,7 @@
  *                   the workload definition's reading.
  *   Q5_0, Q5_1,     layouts not on the pages (ggml's, a reading): pinned by
  *   ggml q8_0, Q2_K hand-built blocks and mutations; Q2_K also by the page's 84
- *                   bytes per 256 weights. "Parity unpinned" against the pages
+ *   Q5_K, Q3_K      bytes per 256 weights. "Parity unpinned" against the pages
  *                   for the bit placements.
  *   GEMV            pinned: exact rational sums on tiny inputs, unit-vector
  *                   columns (catches a transposed operand), closed forms.
@@ -48,7 +48,7 @@
 #include <string.h>
 
 enum { ORC_Q4_0 = 1, ORC_Q8_0 = 2, ORC_Q4_K = 3, ORC_Q6_K = 4, ORC_Q5_0 = 5, ORC_Q5_1 = 6, ORC_Q8_0G = 7,
-       ORC_Q2_K = 8 };
+       ORC_Q2_K = 8, ORC_Q5_K = 9, ORC_Q3_K = 10 };
 
 /* ---- IEEE-754 binary16 -> binary32, from the format definition ---------------
  * sign s (1 bit), exponent e (5 bits, bias 15), fraction f (10 bits):
@@ -233,6 +233,54 @@ void orc_dequant_q2_K_block(const uint8_t *blk, float *out) {
     }
 }
 
+/* Q5_K: 176 bytes -> 256 weights: fp16 d, fp16 dmin, the 12-byte scale/min
+ * field of Q4_K (same packing), qh[32], qs[128]. Element e = 64c + 32h + l
+ * (c = 0..3, h = 0 low / 1 high, l = 0..31): its four low bits are the low (h =
+ * 0) or high (h = 1) nibble of qs[32c + l], its fifth bit is bit 2c + h of
+ * qh[l]; sub-block 2c + h. Value, left to right: (d * sc) * q - (dmin * mn),
+ * q in 0..31 (d * sc * q is exact: 11 + 6 + 5 bits).                           */
+void orc_dequant_q5_K_block(const uint8_t *blk, float *out) {
+    const float dmin = rd_fp16(blk + 2), d = rd_fp16(blk);
+    const uint8_t *fields = blk + 4, *qh = blk + 16, *qs = blk + 48;
+    for (int e = 0; e < 256; ++e) {
+        int c = e / 64, h = (e % 64) / 32, l = e % 32, sb = 2 * c + h;
+        int sc, mn;
+        orc_q4k_scale_min(fields, sb, &sc, &mn);
+        int nib = h ? (qs[32 * c + l] >> 4) : (qs[32 * c + l] & 15);
+        int q = nib | (((qh[l] >> sb) & 1) << 4);
+        float a = d * (float)sc;
+        a = a * (float)q;
+        float b = dmin * (float)mn;
+        out[e] = a - b;
+    }
+}
+
+/* Q3_K: 110 bytes -> 256 weights: hmask[32], qs[64] of 2-bit quants, 12 bytes of
+ * sixteen 6-bit scales, fp16 d at byte 108. Element e = 128n + 32j + l (n = half,
+ * j = 0..3, l = 0..31): q = (bits 2j..2j+1 of qs[32n + l]) - 4 when bit 4n + j of
+ * hmask[l] is clear (else - 0), so q in -4..3; sub-block s = 8n + 2j + l/16 of
+ * 16 weights. Scale s: low four bits in byte s (s < 8, low nibble) or byte s - 8
+ * (s >= 8, high nibble) of the field, top two bits at bit 2 (s / 4) of byte
+ * 8 + s % 4; the scale is that 6-bit value minus 32. Value: (d * scale) * q,
+ * exact (11 + 6 + 3 bits).                                                      */
+static int q3k_scale(const uint8_t *f, int s) {
+    int low = s < 8 ? (f[s] & 15) : (f[s - 8] >> 4);
+    int high = (f[8 + s % 4] >> (2 * (s / 4))) & 3;
+    return (low | (high << 4)) - 32;
+}
+
+void orc_dequant_q3_K_block(const uint8_t *blk, float *out) {
+    const uint8_t *hmask = blk, *qs = blk + 32, *f = blk + 96;
+    float d = rd_fp16(blk + 108);
+    for (int e = 0; e < 256; ++e) {
+        int n = e / 128, j = (e % 128) / 32, l = e % 32;
+        int low2 = (qs[32 * n + l] >> (2 * j)) & 3;
+        int q = ((hmask[l] >> (4 * n + j)) & 1) ? low2 : low2 - 4;
+        float a = d * (float)q3k_scale(f, 8 * n + 2 * j + l / 16);
+        out[e] = a * (float)q;
+    }
+}
+
 int orc_block_bytes(int type) {
     switch (type) {
     case ORC_Q4_0: return 18;
@@ -243,6 +291,8 @@ int orc_block_bytes(int type) {
     case ORC_Q5_1: return 24;
     case ORC_Q8_0G: return 34;
     case ORC_Q2_K: return 84;
+    case ORC_Q5_K: return 176;
+    case ORC_Q3_K: return 110;
     default: return -1;
     }
 }
@@ -250,7 +300,7 @@ int orc_block_bytes(int type) {
 int orc_block_weights(int type) {
     switch (type) {
     case ORC_Q4_0: case ORC_Q8_0: case ORC_Q5_0: case ORC_Q5_1: case ORC_Q8_0G: return 32;
-    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q2_K: return 256;
+    case ORC_Q4_K: case ORC_Q6_K: case ORC_Q2_K: case ORC_Q5_K: case ORC_Q3_K: return 256;
     default: return -1;
     }
 }
@@ -272,6 +322,8 @@ int orc_dequant(int type, const uint8_t *blocks, int64_t n, float *out) {
         case ORC_Q5_1: orc_dequant_q5_1_block(blk, o); break;
         case ORC_Q8_0G: orc_dequant_q8_0g_block(blk, o); break;
         case ORC_Q2_K: orc_dequant_q2_K_block(blk, o); break;
+        case ORC_Q5_K: orc_dequant_q5_K_block(blk, o); break;
+        case ORC_Q3_K: orc_dequant_q3_K_block(blk, o); break;
         }
     }
     return 0;

@@ -33,16 +33,21 @@ Q8_0 = 2  # PETIT q8_0: fp32 scale + 32 int8
 Q4_K = 3
 Q6_K = 4
 # More GGUF block formats (ggml layouts): Q5_0 (22 B / 32), Q5_1 (24 B / 32),
-# ggml's q8_0 with an fp16 scale (34 B / 32), Q2_K (84 B / 256).
+# ggml's q8_0 with an fp16 scale (34 B / 32), Q2_K (84 B / 256), Q5_K (176 B /
+# 256), Q3_K (110 B / 256).
 Q5_0 = 5
 Q5_1 = 6
 Q8_0G = 7
 Q2_K = 8
+Q5_K = 9
+Q3_K = 10
 
 TYPE_NAMES = {Q4_0: "q4_0", Q8_0: "q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q5_0: "Q5_0", Q5_1: "Q5_1",
-              Q8_0G: "q8_0 (ggml)", Q2_K: "Q2_K"}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210, Q5_0: 22, Q5_1: 24, Q8_0G: 34, Q2_K: 84}
-BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_0: 32, Q5_1: 32, Q8_0G: 32, Q2_K: 256}
+              Q8_0G: "q8_0 (ggml)", Q2_K: "Q2_K", Q5_K: "Q5_K", Q3_K: "Q3_K"}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 36, Q4_K: 144, Q6_K: 210, Q5_0: 22, Q5_1: 24, Q8_0G: 34, Q2_K: 84, Q5_K: 176,
+               Q3_K: 110}
+BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256, Q5_0: 32, Q5_1: 32, Q8_0G: 32, Q2_K: 256, Q5_K: 256,
+                 Q3_K: 256}
 
 SCALE_LO, SCALE_HI = 1e-4, 1e-2
 
@@ -59,12 +64,15 @@ def gen_blocks(qtype: int, nblocks: int, rng: np.random.Generator) -> np.ndarray
     """Return `nblocks` random blocks of `qtype` as a flat uint8 array."""
     bb = BLOCK_BYTES[qtype]
     out = np.empty((nblocks, bb), dtype=np.uint8)
-    if qtype == Q4_K:
+    if qtype in (Q4_K, Q5_K):  # fp16 d, dmin, then scale/min fields and quant bytes
         d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
         dmin = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
         out[:, 0:2] = _fp16_bytes(d)
         out[:, 2:4] = _fp16_bytes(dmin)
-        out[:, 4:144] = rng.integers(0, 256, (nblocks, 140), dtype=np.uint8)
+        out[:, 4:bb] = rng.integers(0, 256, (nblocks, bb - 4), dtype=np.uint8)
+    elif qtype == Q3_K:  # hmask, 2-bit quants, scale fields, then fp16 d
+        out[:, 0:108] = rng.integers(0, 256, (nblocks, 108), dtype=np.uint8)
+        out[:, 108:110] = _fp16_bytes(rng.uniform(SCALE_LO, SCALE_HI, nblocks))
     elif qtype == Q6_K:
         d = rng.uniform(SCALE_LO, SCALE_HI, nblocks)
         out[:, 0:208] = rng.integers(0, 256, (nblocks, 208), dtype=np.uint8)
@@ -109,9 +117,11 @@ def gen_blocks_full_range(qtype: int, nblocks: int, rng: np.random.Generator) ->
         out[:, col] = (h & 0xFF).astype(np.uint8)
         out[:, col + 1] = (h >> 8).astype(np.uint8)
 
-    if qtype == Q4_K:
+    if qtype in (Q4_K, Q5_K):
         clamp_fp16(0)
         clamp_fp16(2)
+    elif qtype == Q3_K:
+        clamp_fp16(108)
     elif qtype == Q6_K:
         clamp_fp16(208)
     elif qtype in (Q4_0, Q5_0, Q8_0G):
