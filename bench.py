@@ -54,16 +54,22 @@ WORKLOADS = {
     "ffn_q5_1": "Q5_1 GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
     "ffn_q8_0g": "ggml q8_0 (fp16 scale) GEMV 5632x2048 (ffn_gate/up shape)",
     "ffn_q2k": "Q2_K GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
+    "ffn_q5k": "Q5_K GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
+    "ffn_q3k": "Q3_K GEMV 5632x2048 (ffn_gate/up shape; ggml layout)",
     "dequant_q4k": "standalone dequantisation, Q4_K, 2^27 weights -> fp32",
     "dequant_q6k": "standalone dequantisation, Q6_K, 2^27 weights -> fp32",
     "dequant_q8_0": "standalone dequantisation, PETIT q8_0, 2^27 weights -> fp32",
     "dequant_q4_0": "standalone dequantisation, PETIT q4_0, 2^27 weights -> fp32",
     "dequant_q5_1": "standalone dequantisation, Q5_1 (ggml layout), 2^27 weights -> fp32",
     "dequant_q2k": "standalone dequantisation, Q2_K (ggml layout), 2^27 weights -> fp32",
+    "dequant_q5k": "standalone dequantisation, Q5_K (ggml layout), 2^27 weights -> fp32",
+    "dequant_q3k": "standalone dequantisation, Q3_K (ggml layout), 2^27 weights -> fp32",
 }
-MORE_GEMV = {"ffn_q5_0": synth.Q5_0, "ffn_q5_1": synth.Q5_1, "ffn_q8_0g": synth.Q8_0G, "ffn_q2k": synth.Q2_K}
+MORE_GEMV = {"ffn_q5_0": synth.Q5_0, "ffn_q5_1": synth.Q5_1, "ffn_q8_0g": synth.Q8_0G, "ffn_q2k": synth.Q2_K,
+             "ffn_q5k": synth.Q5_K, "ffn_q3k": synth.Q3_K}
 DEQUANT_TYPES = {"dequant_q4k": synth.Q4_K, "dequant_q6k": synth.Q6_K, "dequant_q8_0": synth.Q8_0,
-                 "dequant_q4_0": synth.Q4_0, "dequant_q5_1": synth.Q5_1, "dequant_q2k": synth.Q2_K}
+                 "dequant_q4_0": synth.Q4_0, "dequant_q5_1": synth.Q5_1, "dequant_q2k": synth.Q2_K,
+                 "dequant_q5k": synth.Q5_K, "dequant_q3k": synth.Q3_K}
 DEQUANT_N = 1 << 27  # weights per dequantisation step: in + out bytes are several times L2
 
 

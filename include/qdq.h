@@ -30,7 +30,18 @@
  *                  weights, 64 bytes of 2-bit quants (weight 128n + 32j + l: bits
  *                  2j..2j+1 of byte 32n + l, pair 8n + 2j + l/16), fp16 d, fp16
  *                  dmin. w = d*sc*q - dmin*mn.
- *   These four are decoded by qdq_dequant and multiplied by qdq_gemv (a
+ *   QDQ_Q5_K       176 bytes per 256: fp16 d, fp16 dmin, the 12 scale/min bytes
+ *                  of Q4_K (same packing), qh[32], qs[128]. Weight 64c + 32h + l:
+ *                  low four bits in the low (h = 0) or high (h = 1) nibble of
+ *                  qs[32c + l], fifth bit at bit 2c + h of qh[l]; sub-block 2c + h.
+ *                  w = d*sc*q - dmin*mn, q in 0..31.
+ *   QDQ_Q3_K       110 bytes per 256: hmask[32], qs[64], 12 bytes of sixteen
+ *                  6-bit scales, fp16 d. Weight 128n + 32j + l: bits 2j..2j+1 of
+ *                  qs[32n + l], minus 4 unless bit 4n + j of hmask[l] is set;
+ *                  scale s = 8n + 2j + l/16 keeps its low four bits in byte s
+ *                  (s < 8, low nibble) or s - 8 (high nibble), its top two at
+ *                  bit 2(s/4) of byte 8 + s%4. w = d*(scale - 32)*q.
+ *   These six are decoded by qdq_dequant and multiplied by qdq_gemv (a
  *   separate exact-per-weight kernel, any batch); groups and plans take the
  *   main four only (QDQ_ERR_TYPE).
  *
@@ -68,7 +79,7 @@ typedef struct CUstream_st *qdq_stream_t; /* == cudaStream_t */
 enum qdq_type {
     QDQ_Q4_0 = 1, QDQ_Q8_0 = 2, QDQ_Q4_K = 3, QDQ_Q6_K = 4,
     /* More GGUF formats (see the notes below the main four): */
-    QDQ_Q5_0 = 5, QDQ_Q5_1 = 6, QDQ_Q8_0_GGML = 7, QDQ_Q2_K = 8
+    QDQ_Q5_0 = 5, QDQ_Q5_1 = 6, QDQ_Q8_0_GGML = 7, QDQ_Q2_K = 8, QDQ_Q5_K = 9, QDQ_Q3_K = 10
 };
 
 enum qdq_status {
@@ -333,7 +344,8 @@ int qdq_quantize(int type, const float *x, int64_t n, void *blocks, qdq_stream_t
  * more) with the tensors' names, dims (dims[0] innermost: the row length),
  * GGUF type code, the library type that decodes it (QDQ_Q4_0 for type 2,
  * QDQ_Q5_0 for 6, QDQ_Q5_1 for 7, QDQ_Q8_0_GGML for 8, QDQ_Q2_K for 10,
- * QDQ_Q4_K for 12, QDQ_Q6_K for 14, else 0), absolute byte offset and size.
+ * QDQ_Q3_K for 11, QDQ_Q4_K for 12, QDQ_Q5_K for 13, QDQ_Q6_K for 14, else 0),
+ * absolute byte offset and size.
  * qdq_gguf_find_kv locates a metadata value: its GGUF value type and the byte
  * offset of the value (QDQ_ERR_NOT_FOUND if the key is absent).
  * ------------------------------------------------------------------------- */

@@ -110,10 +110,11 @@ QDQ_DEV uint32_t ldg_u32_a2(const uint8_t *p) { return ldg_u16(p) | (ldg_u16(p +
 // Block geometry of every format the decoder knows.
 __host__ __device__ constexpr int fmt_bytes(int t) {
     return t == QDQ_Q4_K ? 144 : t == QDQ_Q6_K ? 210 : t == QDQ_Q8_0 ? 36 : t == QDQ_Q4_0 ? 18 : t == QDQ_Q5_0 ? 22
-           : t == QDQ_Q5_1 ? 24 : t == QDQ_Q8_0_GGML ? 34 : t == QDQ_Q2_K ? 84 : 0;
+           : t == QDQ_Q5_1 ? 24 : t == QDQ_Q8_0_GGML ? 34 : t == QDQ_Q2_K ? 84 : t == QDQ_Q5_K ? 176
+           : t == QDQ_Q3_K ? 110 : 0;
 }
 __host__ __device__ constexpr int fmt_weights(int t) {
-    return (t == QDQ_Q4_K || t == QDQ_Q6_K || t == QDQ_Q2_K) ? 256 : 32;
+    return (t == QDQ_Q4_K || t == QDQ_Q6_K || t == QDQ_Q2_K || t == QDQ_Q5_K || t == QDQ_Q3_K) ? 256 : 32;
 }
 
 // Weights e0 .. e0+3 (e0 a multiple of 4) of the block at `blk`.
@@ -190,6 +191,39 @@ QDQ_DEV float4 decode4(const uint8_t *blk, int e0) {
         v.y = __fsub_rn(__fmul_rn(dl, (float)((q >> 8) & 3)), ml);
         v.z = __fsub_rn(__fmul_rn(dl, (float)((q >> 16) & 3)), ml);
         v.w = __fsub_rn(__fmul_rn(dl, (float)((q >> 24) & 3)), ml);
+    } else if constexpr (TYPE == QDQ_Q5_K) {  // blk 16-byte aligned
+        // the Q4_K header; weight 64c + 32h + l: nibble h of qs[32c + l], fifth
+        // bit at bit 2c + h of qh[l]; (d * sc) * q - (dmin * mn)
+        const uint4 H = __ldg((const uint4 *)blk);
+        const int c = e0 >> 6, h = (e0 >> 5) & 1, l = e0 & 31;
+        uint32_t sc2, mn2;
+        q4k_pair_fields(H.y, H.z, H.w, c, &sc2, &mn2);
+        const uint32_t sc = h ? (sc2 >> 8) : (sc2 & 0xFF);
+        const uint32_t mn = h ? (mn2 >> 8) : (mn2 & 0xFF);
+        const float d = half_bits_to_float(H.x & 0xFFFF), dmin = half_bits_to_float(H.x >> 16);
+        const uint32_t q = ldg_u32(blk + 48 + 32 * c + l) >> (4 * h);
+        const uint32_t qh = ldg_u32(blk + 16 + l) >> (2 * c + h);
+        v.x = q4k_weight(d, dmin, sc, mn, (q & 15) | ((qh & 1) << 4));
+        v.y = q4k_weight(d, dmin, sc, mn, ((q >> 8) & 15) | (((qh >> 8) & 1) << 4));
+        v.z = q4k_weight(d, dmin, sc, mn, ((q >> 16) & 15) | (((qh >> 16) & 1) << 4));
+        v.w = q4k_weight(d, dmin, sc, mn, ((q >> 24) & 15) | (((qh >> 24) & 1) << 4));
+    } else if constexpr (TYPE == QDQ_Q3_K) {  // blk 2-byte aligned
+        // weight 128n + 32j + l: bits 2j..2j+1 of qs[32n + l] minus 4 unless bit
+        // 4n + j of hmask[l] is set; scale s = 8n + 2j + l/16 (6 bits, minus 32);
+        // (d * scale) * q, exact
+        const int n = e0 >> 7, j = (e0 >> 5) & 3, l = e0 & 31, s = 8 * n + 2 * j + (l >> 4);
+        const uint32_t q = ldg_u32_a2(blk + 32 + 32 * n + l) >> (2 * j);
+        const uint32_t hm = ldg_u32_a2(blk + l) >> (4 * n + j);
+        const uint32_t lo = s < 8 ? (__ldg(blk + 96 + s) & 15u) : (__ldg(blk + 96 + s - 8) >> 4);
+        const uint32_t hi = (__ldg(blk + 104 + (s & 3)) >> (2 * (s >> 2))) & 3u;
+        const float dl = __fmul_rn(half_bits_to_float(ldg_u16(blk + 108)), (float)((int)(lo | (hi << 4)) - 32));
+        float w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q2 = (int)((q >> (8 * k)) & 3u);
+            w[k] = __fmul_rn(dl, (float)(((hm >> (8 * k)) & 1u) ? q2 : q2 - 4));
+        }
+        v = make_float4(w[0], w[1], w[2], w[3]);
     } else {  // QDQ_Q4_0, blk 2-byte aligned
         const float d = half_bits_to_float(ldg_u16(blk));
         uint32_t q = ldg_u32_a2(blk + 2 + (e0 & 15));

@@ -4,7 +4,8 @@
 // and a count n in, n floats out); "PicoLM Q6_K quantisation bug"
 // (dequantize_row_q6_K with the is + l/16 scale index); "PETIT" (q8_0, q4_0).
 //
-// Also the further GGUF formats (Q5_0, Q5_1, ggml q8_0, Q2_K; ggml block layouts).
+// Also the further GGUF formats (Q5_0, Q5_1, ggml q8_0, Q2_K, Q5_K, Q3_K; ggml
+// block layouts).
 //
 // One thread produces 4 consecutive weights and writes them with one 16-byte
 // store, so a warp writes 512 contiguous bytes per instruction. The kernel is
@@ -55,6 +56,8 @@ int launch_dequant(int type, const void *blocks, int64_t n, float *out, cudaStre
         case QDQ_Q5_1: dequant_kernel<QDQ_Q5_1><<<grid, threads, 0, stream>>>(src, nquads, out); break;
         case QDQ_Q8_0_GGML: dequant_kernel<QDQ_Q8_0_GGML><<<grid, threads, 0, stream>>>(src, nquads, out); break;
         case QDQ_Q2_K: dequant_kernel<QDQ_Q2_K><<<grid, threads, 0, stream>>>(src, nquads, out); break;
+        case QDQ_Q5_K: dequant_kernel<QDQ_Q5_K><<<grid, threads, 0, stream>>>(src, nquads, out); break;
+        case QDQ_Q3_K: dequant_kernel<QDQ_Q3_K><<<grid, threads, 0, stream>>>(src, nquads, out); break;
         default: return QDQ_ERR_TYPE;
     }
     return cudaGetLastError() == cudaSuccess ? QDQ_OK : QDQ_ERR_CUDA;

@@ -1,5 +1,5 @@
 // qdq_gemv_more.cu -- fused dequant-GEMV for the further GGUF formats (Q5_0,
-// Q5_1, ggml q8_0, Q2_K; ggml block layouts, a reading: the pages name these
+// Q5_1, ggml q8_0, Q2_K, Q5_K, Q3_K; ggml block layouts, a reading: the pages name these
 // formats and give Q2_K's size, "S21 The Capstone: picoLM, in Python", section 2).
 //
 // y[b][r] = sum_c w[r][c] x[b][c] with each weight decoded by the shared decoder
@@ -73,7 +73,8 @@ int launch_type(const uint8_t *W, int64_t rows, int64_t cols, const float *x, fl
 }  // namespace
 
 bool is_more_type(int type) {
-    return type == QDQ_Q5_0 || type == QDQ_Q5_1 || type == QDQ_Q8_0_GGML || type == QDQ_Q2_K;
+    return type == QDQ_Q5_0 || type == QDQ_Q5_1 || type == QDQ_Q8_0_GGML || type == QDQ_Q2_K || type == QDQ_Q5_K ||
+           type == QDQ_Q3_K;
 }
 
 int launch_gemv_more(int type, const void *W, int64_t rows, int64_t cols, const float *x, float *y, int batch,
@@ -91,6 +92,8 @@ int launch_gemv_more(int type, const void *W, int64_t rows, int64_t cols, const 
             case QDQ_Q5_1: rc = launch_type<QDQ_Q5_1>(w, rows, cols, xs, ys, nb, grid, stream); break;
             case QDQ_Q8_0_GGML: rc = launch_type<QDQ_Q8_0_GGML>(w, rows, cols, xs, ys, nb, grid, stream); break;
             case QDQ_Q2_K: rc = launch_type<QDQ_Q2_K>(w, rows, cols, xs, ys, nb, grid, stream); break;
+            case QDQ_Q5_K: rc = launch_type<QDQ_Q5_K>(w, rows, cols, xs, ys, nb, grid, stream); break;
+            case QDQ_Q3_K: rc = launch_type<QDQ_Q3_K>(w, rows, cols, xs, ys, nb, grid, stream); break;
             default: return QDQ_ERR_TYPE;
         }
         if (rc) return rc;

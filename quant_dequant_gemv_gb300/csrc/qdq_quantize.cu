@@ -153,9 +153,9 @@ void ggml_geometry(uint32_t t, int *bb, int *bw, int *qdq_type) {
         case 7: *bb = 24, *bw = 32, *qdq_type = QDQ_Q5_1; break;     // q5_1
         case 8: *bb = 34, *bw = 32, *qdq_type = QDQ_Q8_0_GGML; break;  // ggml q8_0 (fp16 scale)
         case 10: *bb = 84, *bw = 256, *qdq_type = QDQ_Q2_K; break;   // q2_K
-        case 11: *bb = 110, *bw = 256; break;                        // q3_K
+        case 11: *bb = 110, *bw = 256, *qdq_type = QDQ_Q3_K; break;  // q3_K
         case 12: *bb = 144, *bw = 256, *qdq_type = QDQ_Q4_K; break;  // q4_K
-        case 13: *bb = 176, *bw = 256; break;                        // q5_K
+        case 13: *bb = 176, *bw = 256, *qdq_type = QDQ_Q5_K; break;  // q5_K
         case 14: *bb = 210, *bw = 256, *qdq_type = QDQ_Q6_K; break;  // q6_K
         default: *bb = 0, *bw = 1; break;
     }

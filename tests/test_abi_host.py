@@ -55,7 +55,7 @@ def test_argument_checks_precede_device_work(lib):
     assert lib.qdq_gemv(3, 0, 4, 256, 0, 0, 0, 0) == -2            # batch < 1
     assert lib.qdq_gemv(3, 0, 0, 256, 0, 0, 1, 0) == 0             # rows == 0: no-op
     assert lib.qdq_dequant(4, 0, 100, 0) == -2                      # n % 256
-    assert lib.qdq_dequant(9, 0, 256, 0) == -1
+    assert lib.qdq_dequant(99, 0, 256, 0) == -1
     assert lib.qdq_dequant(1, 0, 0, 0) == 0                         # n == 0: no-op
     assert lib.qdq_gemv_group(None, 9, 1, 0) == -8                  # more than 8 GEMVs
     assert lib.qdq_plan_create(None, None, 1, 1, None) == -4

@@ -86,7 +86,8 @@ def test_malformed_files_are_rejected(q):
 
 def test_further_formats_map_to_their_decoders(q):
     f = gf.build([], [("a", [32, 1], 6, bytes(22)), ("b", [32, 1], 7, bytes(24)), ("c", [32, 1], 8, bytes(34)),
-                      ("d", [256, 1], 10, bytes(84)), ("e", [256, 1], 13, bytes(176))])
+                      ("d", [256, 1], 10, bytes(84)), ("e", [256, 1], 13, bytes(176)),
+                      ("g", [256, 1], 11, bytes(110)), ("h", [32, 1], 3, bytes(20))])
     t, _, _ = q.gguf_parse(f)
-    assert [x["qdq_type"] for x in t] == [synth.Q5_0, synth.Q5_1, synth.Q8_0G, synth.Q2_K, 0]
-    assert [x["bytes"] for x in t] == [22, 24, 34, 84, 176]
+    assert [x["qdq_type"] for x in t] == [synth.Q5_0, synth.Q5_1, synth.Q8_0G, synth.Q2_K, synth.Q5_K, synth.Q3_K, 0]
+    assert [x["bytes"] for x in t] == [22, 24, 34, 84, 176, 110, 20]

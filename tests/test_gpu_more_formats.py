@@ -1,4 +1,4 @@
-"""Q5_0, Q5_1, ggml q8_0 and Q2_K on the GPU against the oracle (ggml block
+"""Q5_0, Q5_1, ggml q8_0, Q2_K, Q5_K and Q3_K on the GPU against the oracle (ggml block
 layouts, a reading: the pages name the formats and give Q2_K's size).
 
 * Dequantisation bit for bit, on the workload draws and on full-range bytes.
@@ -16,7 +16,7 @@ from quant_dequant_gemv_gb300 import synth
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-TYPES = [synth.Q5_0, synth.Q5_1, synth.Q8_0G, synth.Q2_K]
+TYPES = [synth.Q5_0, synth.Q5_1, synth.Q8_0G, synth.Q2_K, synth.Q5_K, synth.Q3_K]
 
 
 @pytest.fixture(scope="module")
