@@ -93,7 +93,10 @@ enum qdq_status {
     QDQ_ERR_DEVICE = -7,   /* current device is not sm_103 */
     QDQ_ERR_LIMIT = -8,    /* more GEMVs or levels than a plan supports */
     QDQ_ERR_FORMAT = -9,   /* a malformed or truncated GGUF file */
-    QDQ_ERR_NOT_FOUND = -10 /* no such GGUF metadata key */
+    QDQ_ERR_NOT_FOUND = -10, /* no such GGUF metadata key */
+    QDQ_ERR_BOUNDS = -11     /* debug builds (-DQDQ_DEBUG) only: a device-side index or
+                                alignment check failed and the access was skipped
+                                (from qdq_get_device_status) */
 };
 
 /* Bytes per block and weights per block of a type; -1 for an unknown type. */

@@ -138,6 +138,7 @@ const char *qdq_status_string(int status) {
         case QDQ_ERR_LIMIT: return "too many GEMVs or levels for a plan, or batch too large for it";
         case QDQ_ERR_FORMAT: return "malformed or truncated GGUF data";
         case QDQ_ERR_NOT_FOUND: return "no such GGUF metadata key";
+        case QDQ_ERR_BOUNDS: return "device-side index or alignment check failed (debug build)";
         default: return "unknown status";
     }
 }

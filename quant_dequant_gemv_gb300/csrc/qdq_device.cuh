@@ -29,6 +29,16 @@ QDQ_DEV int load_volatile(const int *p) { return *(const volatile int *)p; }
 
 QDQ_DEV void record_status(int *status, int code) { atomicCAS(status, 0, code); }
 
+// Device-side index and alignment checks of debug builds (-DQDQ_DEBUG), the
+// stand-in for a memory checker: a failed check records QDQ_ERR_BOUNDS in the
+// kernel's status word and yields false, and the caller skips the access (never
+// a trap). Release builds compile every check to true.
+#ifdef QDQ_DEBUG
+#define QDQ_CHECK(status, cond) ((cond) ? true : (::qdq::record_status((status), QDQ_ERR_BOUNDS), false))
+#else
+#define QDQ_CHECK(status, cond) true
+#endif
+
 // ---- mbarrier ----------------------------------------------------------------
 QDQ_DEV void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -538,13 +538,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int hb = 0; hb < nh_u; ++hb)
                         for (int m = 0; m < a.g; ++m) {
                             const int64_t off = (int64_t)m * a.row_bytes + (int64_t)u * kUnitBytes + hb * kKbh * kBB;
-                            tma_load_2d(stage + hb * a.half_bytes + m * a.region_bytes, &wmap, (int)(off & ~(int64_t)15),
-                                        y, raw_full + 8 * s, pol);
+                            const uint32_t dst_t = stage + hb * a.half_bytes + m * a.region_bytes;
+                            // debug builds: a 16-byte aligned destination and x coordinate
+                            if (QDQ_CHECK(status, (dst_t & 15u) == 0 && ((off & ~(int64_t)15) & 15) == 0))
+                                tma_load_2d(dst_t, &wmap, (int)(off & ~(int64_t)15), y, raw_full + 8 * s, pol);
                         }
                 }
             }
             __syncwarp();
-            if (nbytes) bulk_g2s_hint(dst, (const void *)src_al, nbytes, raw_full + 8 * s, pol);
+            if (nbytes && QDQ_CHECK(status, ((dst | (uint32_t)(uintptr_t)src_al | nbytes) & 15u) == 0))
+                bulk_g2s_hint(dst, (const void *)src_al, nbytes, raw_full + 8 * s, pol);
         }
     } else if (warp == kWarpX) {
         // ---- split X. Sub-chunk j's fp32 x (64 columns of each batch row, fewer for

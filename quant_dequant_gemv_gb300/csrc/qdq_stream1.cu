@@ -860,6 +860,7 @@ QDQ_DEV void tile_slices_b(const Tile &tl, const DevDesc &d, const uint8_t *stag
     const int n = tl.nrows;
     bool fresh = tl.first;
     for (int k = k0; k < kend; k += Cfg<BT>::kCW) {
+        if (!QDQ_CHECK(&s_status_s1, (k >> 3) >= tl.xw0 && (k >> 3) < tl.xw0 + tl.xwn)) break;  // debug builds
         const float *chunk = xbuf + ((k >> 3) - tl.xw0) * stride;
         const float *xs = chunk + slot * BT * kChunk + (k & 7) * kSlice;
         const int kcols = d.cols - k * kSlice;
@@ -907,6 +908,8 @@ QDQ_DEV void tile_units1_nr(const Tile &tl, const DevDesc &d, const uint8_t *sta
             if (p >= npass) break;
         }
         const int k = tl.whole ? kk : kSlicesPerChunk * tl.chunk + kk;  // slice of the row
+        // debug builds: the slice's x chunk inside the staged window
+        if (!QDQ_CHECK(&s_status_s1, (k >> 3) >= tl.xw0 && (k >> 3) < tl.xw0 + tl.xwn)) continue;
         const float *chunk = xbuf + ((k >> 3) - tl.xw0) * stride;
         const float *xs = chunk + slot * kChunk + (k & 7) * kSlice;
         const int kcols = d.cols - k * kSlice;
@@ -1087,6 +1090,8 @@ QDQ_DEV void attend(const A &a, const DevDesc &d, const DescEx &ex, const Tile &
     // chunks of eight: each warp's first chunk is copied here (after wacc)
     uint8_t *kv_area = reinterpret_cast<uint8_t *>(wacc + NCW * 64) + cw * kKVAreaBytes;
     constexpr int kPer2 = kAttnMaxD / 64;
+    // debug builds: the heads inside the level's, a position inside the cache
+    if (!QDQ_CHECK(&s_status_s1, tl.row0 + tl.nrows <= d.rows && pos >= 0 && D <= kAttnMaxD)) return;
     for (int h = (int)tl.row0; h < (int)tl.row0 + tl.nrows; ++h) {
         const int g = h / kv_mul;
         const bool writer = h % kv_mul == 0;
@@ -1281,6 +1286,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 if (ptile == 0) S1_TR(plevel, 29);
                 const uint32_t bytes = tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols);
                 const uint32_t o = ring_place<BT>(next, bytes);
+                // debug builds: the tile lies inside the ring at a 16-byte offset
+                const bool placed = QDQ_CHECK(status, o + bytes <= (uint32_t)Cfg<BT>::kRingBytes && (o & 15u) == 0);
                 for (;;) {
                     bool block = rel < t && rel <= t - kSlots;
                     for (int j = rel; !block && j < t; ++j) {
@@ -1295,9 +1302,9 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 toff[s] = o;
                 tlen[s] = bytes;
                 const uint32_t stage = ring_a + o, bar = full_a + 8 * s;
-                const uint32_t nb = tile_copy(d, tl, stage, bar, kTail);
+                const uint32_t nb = placed ? tile_copy(d, tl, stage, bar, kTail) : 0u;
                 mbar_arrive_expect_tx(bar, nb);  // releases the tail stores above
-                tile_copy(d, tl, stage, bar, kBulk);
+                if (placed) tile_copy(d, tl, stage, bar, kBulk);
                 if (ptile < 2) S1_TR(plevel, 30 + ptile);
                 ++ptile;
                 ++t;
@@ -1445,7 +1452,8 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                 if (buf_rows + tl.nrows > kBufRows || (!tl.first_win && buf_rows > 0)) flush();
                 rg_base = buf_rows;
                 buf_rows += tl.nrows;
-                if (cw == 0)
+                const bool rows_ok = QDQ_CHECK(status, rg_base + tl.nrows <= kBufRows);  // debug builds
+                if (cw == 0 && rows_ok)
                     for (int i = lane; i < tl.nrows; i += 32) {
                         dst[rg_base + i] = (uint64_t)(uintptr_t)(d.y + tl.row0 + i) |
                                            ((tl.first_win && desc_yop(d) != QDQ_Y_ADD) ? 0u : 1u) |
@@ -1459,20 +1467,25 @@ __global__ void __launch_bounds__(Cfg<BT>::kThreads, 1) stream1_kernel(const __g
                             dstride[rg_base + i] = (int)d.rows;
                     }
                 if constexpr (BT == 1) {  // batch 1 adds every unit into the warp's column
-                    for (int i = lane; i < tl.nrows; i += 32) mypart[rg_base + i] = 0.f;
+                    for (int i = lane; rows_ok && i < tl.nrows; i += 32) mypart[rg_base + i] = 0.f;
                     __syncwarp();
                 }
             }
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 5);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 8 + 3 * tiles_in_level);
             const uint32_t toffs = ring_place<BT>(ring_next, tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols));
+            // debug builds: the tile inside the ring, its rows inside the matrix and
+            // the row group inside the partial buffer
+            const bool tile_ok =
+                QDQ_CHECK(status, toffs + tile_ring_bytes(d, tl.nrows, tl.whole, tl.ccols) <= (uint32_t)Cfg<BT>::kRingBytes) &&
+                QDQ_CHECK(status, tl.row0 + tl.nrows <= d.rows && rg_base + tl.nrows <= kBufRows);
             const int s = t % kSlots;
             mbar_wait(full_a + 8 * s, (t / kSlots) & 1, status);
             if (cw == 0 && lane == 0 && tiles_in_level == 0) S1_TR(cur_level, 6);
             if (cw == 0 && lane == 0 && tiles_in_level < 7) S1_TRC(cur_level, 9 + 3 * tiles_in_level);
             ++tiles_in_level;
 
-            {
+            if (tile_ok) {
                 const uint8_t *stage_p = smem + toffs;
                 RowGeo geo;
                 geo.rb = d.rb;
